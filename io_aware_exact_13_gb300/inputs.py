@@ -1,0 +1,116 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic. Its tensors feed both the CUDA path and the fp64 oracle,
+so both sides see identical bits.
+
+Recipe (per workload): a CPU ``torch.Generator`` seeded with the workload's
+seed draws, in this order, Q, K and V as fp32 standard normals of shape
+[B, H, N, d]; then, where the workload asks for it, a per-key-row offset
+U(-a, a) of shape [B, H, N, 1] added to K; then an additive fp32 mask of
+shape [B, N, N] whose entries are -inf with probability ``mask_frac`` (0
+otherwise) plus ``round(full_row_frac * N)`` query rows per batch index,
+chosen without replacement, set entirely to -inf. Q, K, V are multiplied by
+``mul`` and finally rounded to the storage dtype (round to nearest even).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str
+    causal: bool
+    scale: float
+    seed: int
+    mul: float = 1.0
+    k_offset: float = 0.0
+    mask_frac: float = 0.0
+    full_row_frac: float = 0.0
+    note: str = field(default="", compare=False)
+
+    @property
+    def has_mask(self) -> bool:
+        return self.mask_frac > 0.0 or self.full_row_frac > 0.0
+
+    @property
+    def flops(self) -> float:
+        """Attention flop count 4*B*H*N^2*d, halved for causal."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "N": self.N, "d": self.d,
+                "dtype": self.dtype, "causal": self.causal, "mask": self.has_mask, "scale": self.scale}
+
+
+# The five workloads of the attention-forward benchmark suite, smallest first.
+WORKLOADS = {
+    "n256_d64_fp32": Workload("n256_d64_fp32", 1, 1, 256, 64, "fp32", False, 1 / 8, 1001,
+                              note="fp32 inputs, no mask, non-causal"),
+    "b4h8_n1024_d64_bf16_causal": Workload("b4h8_n1024_d64_bf16_causal", 4, 8, 1024, 64, "bf16", True, 1 / 8, 1002),
+    "b2h16_n4096_d128_fp16_mask": Workload("b2h16_n4096_d128_fp16_mask", 2, 16, 4096, 128, "fp16", False,
+                                           1 / math.sqrt(128), 1003, mul=1.5, mask_frac=0.10, full_row_frac=0.01,
+                                           note="additive [B,N,N] mask, 10% -inf, ~1% rows fully masked"),
+    "b1h32_n8192_d128_bf16_causal": Workload("b1h32_n8192_d128_bf16_causal", 1, 32, 8192, 128, "bf16", True,
+                                             1 / math.sqrt(128), 1004),
+    "b1h8_n32768_d128_bf16_causal_koff": Workload("b1h8_n32768_d128_bf16_causal_koff", 1, 8, 32768, 128, "bf16",
+                                                  True, 1 / math.sqrt(128), 1005, k_offset=4.0,
+                                                  note="K rows offset by U(-4,4) to stress max rescaling"),
+}
+HEADLINE = "b1h32_n8192_d128_bf16_causal"
+
+
+def make_qkv(B, H, N, d, dtype="bf16", seed=0, mul=1.0, k_offset=0.0, mask_frac=0.0, full_row_frac=0.0,
+             Nk: Optional[int] = None):
+    """Draw (q, k, v, mask_or_None) on the CPU following the recipe above.
+
+    ``Nk`` (default N) sets the key/value length; the mask, if any, is [B, N, Nk].
+    """
+    Nk = N if Nk is None else Nk
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    if k_offset:
+        off = (torch.rand((B, H, Nk, 1), generator=g, dtype=torch.float32) * 2.0 - 1.0) * k_offset
+        k = k + off
+    mask = None
+    if mask_frac > 0.0 or full_row_frac > 0.0:
+        drop = torch.rand((B, N, Nk), generator=g, dtype=torch.float32) < mask_frac
+        mask = torch.zeros((B, N, Nk), dtype=torch.float32)
+        mask[drop] = float("-inf")
+        nfull = int(round(full_row_frac * N))
+        for b in range(B):
+            rows = torch.randperm(N, generator=g)[:nfull]
+            mask[b, rows, :] = float("-inf")
+    if mul != 1.0:
+        q, k, v = q * mul, k * mul, v * mul
+    t = DTYPES[dtype]
+    return q.to(t).contiguous(), k.to(t).contiguous(), v.to(t).contiguous(), mask
+
+
+def make_workload(w: Workload):
+    """(q, k, v, mask_or_None) on the CPU for a named workload."""
+    return make_qkv(w.B, w.H, w.N, w.d, w.dtype, w.seed, w.mul, w.k_offset, w.mask_frac, w.full_row_frac)
+
+
+def sample_rows(total_rows: int, n: int, seed: int = 0) -> torch.Tensor:
+    """n distinct flat row ids in [0, total_rows), sorted, from a seeded generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    n = min(n, total_rows)
+    return torch.randperm(total_rows, generator=g)[:n].sort().values

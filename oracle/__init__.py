@@ -1,0 +1,187 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY. Only the test suite, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg may import this package. The product path (the
+CUDA library and its Python binding) never imports, loads or calls it, and the
+two share no code.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module compiles it with gcc and marshals numpy arrays through ctypes.
+
+Pins (what ties each routine to the pages rather than to itself) are in
+``tests/test_oracle_pins.py``. Sources, by page title and section:
+
+* "FlashAttention: Exact Attention as an IO-Aware Streaming Computation",
+  sections "Problem setting" and "Mathematical structure": the definition and
+  the running (m, l, a) statistics.
+* "FlashAttention" (glossary), sections "Move less data" (additive mask M),
+  "Why a tile can be discarded", "One row, checked two ways" and "Practice":
+  block summaries, their merge and the two worked examples.
+* "IO-aware exact attention", sections "Tile order and on-chip capacity"
+  (causal: keys at or before the query) and "Backward recomputation".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source (gcc, OpenMP, no -march)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "attn_oracle.h"))
+    ):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    ip = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_attn_f64.argtypes = [dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int]
+    lib.oracle_attn_rows_f64.argtypes = lib.oracle_attn_f64.argtypes + [ip, i64]
+    lib.oracle_attn_blockwise_f64.argtypes = lib.oracle_attn_f64.argtypes + [i64]
+    lib.oracle_attn_bwd_f64.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int]
+    lib.oracle_block_summary_f64.argtypes = [dp, dp, i64, i64, dp, dp, dp]
+    lib.oracle_block_summary_f64.restype = None
+    lib.oracle_merge_f64.argtypes = [ctypes.c_double, ctypes.c_double, dp, ctypes.c_double, ctypes.c_double, dp, i64, dp, dp, dp]
+    lib.oracle_merge_f64.restype = None
+    for f in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_blockwise_f64, lib.oracle_attn_bwd_f64,
+              lib.oracle_num_threads):
+        f.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact conversion to a C-contiguous fp64 array (bf16/fp16/fp32 all embed in fp64)."""
+    if hasattr(a, "detach"):  # a torch tensor: widen on the CPU, which is exact
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shapes(q, k, v, mask):
+    B, H, Nq, d = q.shape
+    Bk, Hk, Nk, dk = k.shape
+    if (Bk, Hk, dk) != (B, H, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{q.shape} k{k.shape} v{v.shape}")
+    if mask is not None and mask.shape != (B, Nq, Nk):
+        raise ValueError(f"mask must be [B, Nq, Nk] = {(B, Nq, Nk)}, got {mask.shape}")
+    return B, H, Nq, Nk, d
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def attention(q, k, v, mask=None, scale=None, causal=False):
+    """Materialised fp64 attention. Returns (out [B,H,Nq,d], lse [B,H,Nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    mask = None if mask is None else _f64(mask)
+    B, H, Nq, Nk, d = _shapes(q, k, v, mask)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    out = np.zeros((B, H, Nq, d))
+    lse = np.zeros((B, H, Nq))
+    rc = _load().oracle_attn_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse),
+                                 B, H, Nq, Nk, d, scale, int(bool(causal)))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_f64 failed")
+    return out, lse
+
+
+def attention_rows(q, k, v, rows, mask=None, scale=None, causal=False):
+    """Materialised fp64 attention for flat row ids (b*H + h)*Nq + i.
+    Returns (out [len(rows), d], lse [len(rows)])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    mask = None if mask is None else _f64(mask)
+    B, H, Nq, Nk, d = _shapes(q, k, v, mask)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    out = np.zeros((rows.size, d))
+    lse = np.zeros(rows.size)
+    rc = _load().oracle_attn_rows_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse),
+                                      B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size)
+    if rc != 0:
+        raise RuntimeError("oracle_attn_rows_f64 failed")
+    return out, lse
+
+
+def attention_blockwise(q, k, v, block, mask=None, scale=None, causal=False):
+    """Blockwise (summary + merge) fp64 attention; must equal ``attention``."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    mask = None if mask is None else _f64(mask)
+    B, H, Nq, Nk, d = _shapes(q, k, v, mask)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    out = np.zeros((B, H, Nq, d))
+    lse = np.zeros((B, H, Nq))
+    rc = _load().oracle_attn_blockwise_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse),
+                                           B, H, Nq, Nk, d, scale, int(bool(causal)), int(block))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_blockwise_f64 failed")
+    return out, lse
+
+
+def block_summary(scores, values):
+    """(m, l, u) of one row's block: scores [n], values [n] or [n, dv]."""
+    s = _f64(scores).reshape(-1)
+    vals = _f64(values)
+    vals2 = vals.reshape(s.size, -1)
+    dv = vals2.shape[1]
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    u = np.zeros(dv)
+    _load().oracle_block_summary_f64(_ptr(s), _ptr(np.ascontiguousarray(vals2)), s.size, dv,
+                                     ctypes.byref(m), ctypes.byref(l), _ptr(u))
+    return m.value, l.value, (u if vals.ndim > 1 else u[0])
+
+
+def merge(a, b):
+    """Merge two block summaries (m, l, u) onto their common maximum."""
+    (mA, lA, uA), (mB, lB, uB) = a, b
+    uA1 = np.atleast_1d(_f64(uA))
+    uB1 = np.atleast_1d(_f64(uB))
+    m = ctypes.c_double()
+    l = ctypes.c_double()
+    u = np.zeros(uA1.size)
+    _load().oracle_merge_f64(float(mA), float(lA), _ptr(uA1), float(mB), float(lB), _ptr(uB1), uA1.size,
+                             ctypes.byref(m), ctypes.byref(l), _ptr(u))
+    scalar = np.ndim(uA) == 0
+    return m.value, l.value, (u[0] if scalar else u)
+
+
+def attention_bwd(q, k, v, dout, mask=None, scale=None, causal=False):
+    """fp64 gradients (dq, dk, dv) of sum(dout * attention(q, k, v))."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    mask = None if mask is None else _f64(mask)
+    B, H, Nq, Nk, d = _shapes(q, k, v, mask)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = _load().oracle_attn_bwd_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(dout), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), B, H, Nq, Nk, d, scale, int(bool(causal)))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd_f64 failed")
+    return dq, dk, dv
