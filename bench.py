@@ -1,0 +1,355 @@
+"""Benchmark of the exact tiled attention forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--cpu-sample-s SECONDS]
+
+One step = one forward of the whole path (every query tile of every head) over
+the headline workload B=1, H=32, N=8192, d=128, bf16, causal, with inputs
+already resident in device memory. Q, K, V and O total 268 MB, more than the
+126 MB L2, so no flush is done between steps (stated in ``config``).
+
+``value`` is attention TFLOP/s (4*B*H*N^2*d, halved for causal) summed over all
+ranks; each rank runs its own copy of the workload (independent problems, no
+collective on the data path; weak scaling). ``e2e`` is the same metric through
+the C ABI with pinned host buffers: each step copies Q, K, V host->device and
+O, lse device->host inside the timed region. ``roofline`` compares the kernel's
+algorithmic flops per launch / its CUDA-event duration with the measured dense
+bf16 tensor peak. ``cpu_baseline`` times the fp64 oracle on a bounded sample of
+query rows of the same workload on the host cores (rank 0, N=1 only).
+
+``--impl reference`` times that fp64 oracle as the reference arm (the method's
+pages ship no code to run); its value is a deliberately slow program's rate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from io_aware_exact_13_gb300.inputs import HEADLINE, WORKLOADS, make_workload, sample_rows  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
+UNIT = "TFLOP/s"
+KERNEL_SOURCES = ["io_aware_exact_13_gb300/csrc/fa_fwd_kernel.cuh", "io_aware_exact_13_gb300/csrc/ptx.cuh",
+                  "io_aware_exact_13_gb300/csrc/fa_launch.cuh"]
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured bf16 burst (MEASURED_PEAKS.json)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16 (no measured peak file)"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if
+    it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != kernel_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world, dev=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier(device_ids=[dev.index] if dev is not None and dev.type == "cuda" else None)
+
+
+def max_over_ranks(world, x: float, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, q, k, v, mask, n_rows: int, seed: int):
+    """Time the fp64 oracle on n_rows sampled query rows; return (seconds, flops, threads)."""
+    import oracle
+
+    rows = sample_rows(w.B * w.H * w.N, n_rows, seed).numpy()
+    i = rows % w.N
+    keys = (i + 1) if w.causal else w.N
+    flops = float((4.0 * w.d * keys).sum() if w.causal else 4.0 * w.d * w.N * len(rows))
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    m64 = None if mask is None else mask.double().numpy()
+    t0 = time.perf_counter()
+    oracle.attention_rows(q64, k64, v64, rows, mask=m64, scale=w.scale, causal=w.causal)
+    return time.perf_counter() - t0, flops, oracle.num_threads()
+
+
+def calibrate_rows(w, q, k, v, mask, target_s: float):
+    """Number of sampled rows whose oracle run takes about target_s seconds."""
+    n = 256
+    while True:
+        dt, _, _ = oracle_sample(w, q, k, v, mask, n, seed=99)
+        if dt > 0.5 or n >= w.B * w.H * w.N:
+            return max(1, min(w.B * w.H * w.N, int(n * target_s / max(dt, 1e-6))))
+        n *= 4
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    q, k, v, mask = make_workload(w)
+    # keep the whole reference run to about two minutes of oracle work
+    per_step = min(args.ref_step_s, max(0.2, 120.0 / max(1, args.steps + args.warmup)))
+    n_rows = calibrate_rows(w, q, k, v, mask, per_step)
+    for s in range(args.warmup):
+        oracle_sample(w, q, k, v, mask, n_rows, seed=s)
+    tot_t, tot_f, threads = 0.0, 0.0, 1
+    for s in range(args.steps):
+        dt, fl, threads = oracle_sample(w, q, k, v, mask, n_rows, seed=1000 + s)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = f"{n_rows} uniformly sampled query rows of {w.name} per step (fp64 materialised rows)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": w.describe(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from io_aware_exact_13_gb300 import fa
+
+    entry = {"bf16": fa.fa_fwd, "fp16": fa.fa_fwd_fp16, "fp32": fa.fa_fwd_fp32}[w.dtype]
+    q, k, v, mask = make_workload(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if mask is None else mask.to(dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        entry(qd, kd, vd, md, od, lsed, w.scale, w.causal, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status(stream) != 0:
+        raise SystemExit("device status word set during warm-up")
+
+    # ---------------------------------------------------------------- device-resident timing
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop() if sampler else None
+    total_ms = max_over_ranks(world, t_start.elapsed_time(t_end), dev)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    status = fa.fa_get_device_status(stream)
+    if status != 0:
+        raise SystemExit(f"device status word {status} after the timed region")
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---------------------------------------------------------------- end to end through host buffers
+    qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    mh = None if mask is None else mask.pin_memory()
+    oh = torch.empty(od.shape, dtype=od.dtype).pin_memory()
+    lh = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        if mh is not None:
+            md.copy_(mh, non_blocking=True)
+        step()
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(lsed, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 20))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh) + ((mh,) if mh is not None else ()))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+
+    if rank != 0:
+        return 0
+    peak, peak_src = load_peak()
+    mean_launch_s = statistics.mean(launch_ms) * 1e-3
+    achieved = w.flops / mean_launch_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(w.name), "peak_source": peak_src,
+                "kernel": "fa_fwd_kernel", "launch_ms_mean": 1e3 * mean_launch_s,
+                "launch_ms_min": min(launch_ms), "launch_ms_max": max(launch_ms)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": dict(w.describe(), l2="inputs (Q,K,V,O = 268 MB) exceed the 126 MB L2; no flush between steps",
+                       parallelism=f"replicas x{world} (independent problems, no collective)"),
+        "pct_of_peak": 100.0 * value / (world * peak),
+        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "roofline": roofline,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n_rows = calibrate_rows(w, q, k, v, mask, args.cpu_sample_s)
+        dt, fl, threads = oracle_sample(w, q, k, v, mask, n_rows, seed=12345)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"{n_rows} uniformly sampled query rows of {w.name} "
+                                          f"(fp64 materialised rows, {dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,87 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention forward for GB300 (sm_103a).
+ *
+ * Operation ("FlashAttention: Exact Attention as an IO-Aware Streaming
+ * Computation", sections "Problem setting" and "Mathematical structure";
+ * "FlashAttention" glossary, section "Move less data" for the additive mask M):
+ *
+ *     O = softmax(scale * Q K^T + M) V,   lse_i = ln sum_j exp(s_ij)
+ *
+ * computed exactly (up to floating-point rounding) by streaming key/value
+ * tiles past an on-chip query tile that keeps its running row maximum m,
+ * denominator l and unnormalised accumulator a ("IO-aware exact attention",
+ * section "One tiled forward-pass iteration"). Only O and lse are written to
+ * device memory; no N x N score or probability tensor is ever stored.
+ *
+ * Layouts (all contiguous, row-major, last index fastest; all DEVICE pointers):
+ *   q, k, v, out : [B][H][N][d], element type per entry point (bf16, fp16, fp32);
+ *                  out has the same element type as q.
+ *   lse          : float [B][H][N], natural log of the softmax normaliser of the
+ *                  scaled, masked scores; -inf for a fully masked row.
+ *   mask_or_null : NULL, or float [B][N][N], additive, shared by all H heads;
+ *                  entries finite or -inf (+inf and NaN are not supported).
+ *   causal       : nonzero allows key j for query i iff j <= i ("IO-aware exact
+ *                  attention", section "Tile order and on-chip capacity").
+ *                  Causal and mask combine additively when both are given.
+ *   scale        : multiplies Q K^T (typically 1/sqrt(d)).
+ * A query row whose every key is excluded gets out = 0 and lse = -inf.
+ *
+ * Ownership: every pointer is caller-owned device memory. The library allocates
+ * no device memory, keeps no per-call state and may be called from several
+ * host threads. Calls are stream-ordered and asynchronous: they enqueue work on
+ * `stream` (a cudaStream_t; NULL = legacy default stream) and return.
+ *
+ * Errors: arguments are checked on the host before anything is launched; a
+ * failed check returns the negative status below and launches nothing. A
+ * launch failure returns FA_ERR_LAUNCH. Device-side pipeline waits are bounded:
+ * if one gives up, the kernel records FA_ERR_TIMEOUT in a device status word
+ * (read it with fa_get_device_status) and the outputs are undefined.
+ */
+#ifndef FA_H
+#define FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = -1,        /* a required pointer is NULL */
+    FA_ERR_ALIGN = -2,       /* a pointer is not 16-byte aligned */
+    FA_ERR_SHAPE = -3,       /* B, H or N < 1, or a size overflows */
+    FA_ERR_UNSUPPORTED = -4, /* d not supported for this element type */
+    FA_ERR_LAUNCH = -5,      /* the CUDA launch (or tensor-map encoding) failed */
+    FA_ERR_TIMEOUT = -6      /* a device-side wait gave up (device status word) */
+} fa_status;
+
+/* bf16 Q/K/V/out, fp32 accumulation. d in {64, 128}. */
+int fa_fwd(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
+           float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* fp16 Q/K/V/out, fp32 accumulation. d in {64, 128}. */
+int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
+                float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* fp32 Q/K/V/out. Products run on the tensor cores in TF32 (inputs rounded to
+ * TF32, fp32 accumulation); P is kept in TF32. d = 64 only (d = 128 returns
+ * FA_ERR_UNSUPPORTED: two fp32 query tiles and a K/V ring do not fit in
+ * shared memory). */
+int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
+                float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* Static text for a status code (never NULL). */
+const char *fa_status_string(int status);
+
+/* Synchronises `stream`, returns the device status word of the current device
+ * (FA_OK or FA_ERR_TIMEOUT) and clears it. Returns FA_ERR_LAUNCH if the
+ * synchronisation itself fails. */
+int fa_get_device_status(void *stream);
+
+/* Number of streaming multiprocessors the persistent grid is sized for on the
+ * current device, or a negative status. */
+int fa_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_H */

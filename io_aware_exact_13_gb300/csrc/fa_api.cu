@@ -1,0 +1,181 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, the device
+// status word, tensor-map encoding, and dispatch to the per-type launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_launch.cuh"
+
+namespace fa {
+int launch_fwd_bf16(const LaunchArgs &a);
+int launch_fwd_fp16(const LaunchArgs &a);
+int launch_fwd_fp32(const LaunchArgs &a);
+}  // namespace fa
+
+// Device status word: FA_OK, or FA_ERR_TIMEOUT once any bounded wait gave up.
+__device__ int g_fa_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per pipeline wait
+
+struct DeviceInfo {
+    std::once_flag once;
+    int num_sms = -1;
+    int *status = nullptr;
+    bool ok = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// Per-device set-up, once: SM count and the device address of the status word.
+DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    DeviceInfo &di = g_dev[dev];
+    std::call_once(di.once, [&di, dev] {
+        int sms = 0;
+        void *addr = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return;
+        if (cudaGetSymbolAddress(&addr, g_fa_status) != cudaSuccess || addr == nullptr) return;
+        di.num_sms = sms;
+        di.status = static_cast<int *>(addr);
+        di.ok = true;
+    });
+    return di.ok ? &di : nullptr;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+enum class Type { BF16, FP16, FP32 };
+
+int check_args(Type ty, const void *q, const void *k, const void *v, const float *mask, const void *out,
+               const float *lse, int B, int H, int N, int d) {
+    if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        (mask && !aligned(mask, 16)))
+        return FA_ERR_ALIGN;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (bh > INT32_MAX) return FA_ERR_SHAPE;
+    const int64_t items = bh * ((static_cast<int64_t>(N) + 255) / 256);
+    if (items > INT32_MAX) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (ty == Type::FP32 && d != 64) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+int fwd_common(Type ty, const void *q, const void *k, const void *v, const float *mask, void *out, float *lse,
+               int B, int H, int N, int d, float scale, int causal, void *stream) {
+    int rc = check_args(ty, q, k, v, mask, out, lse, B, H, N, d);
+    if (rc != FA_OK) return rc;
+    DeviceInfo *di = device_info();
+    if (!di || !encoder()) return FA_ERR_LAUNCH;
+    fa::LaunchArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.mask = mask;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status = di->status;
+    a.num_sms = di->num_sms;
+    a.timeout_ns = kDefaultTimeoutNs;
+    switch (ty) {
+        case Type::BF16: rc = fa::launch_fwd_bf16(a); break;
+        case Type::FP16: rc = fa::launch_fwd_fp16(a); break;
+        case Type::FP32: rc = fa::launch_fwd_fp32(a); break;
+    }
+    return rc;
+}
+
+}  // namespace
+
+namespace fa {
+bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d, int N,
+                     int BH) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                             static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse, int B,
+           int H, int N, int d, float scale, int causal, void *stream) {
+    return fwd_common(Type::BF16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
+}
+
+int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
+                int B, int H, int N, int d, float scale, int causal, void *stream) {
+    return fwd_common(Type::FP16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
+}
+
+int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
+                int B, int H, int N, int d, float scale, int causal, void *stream) {
+    return fwd_common(Type::FP32, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
+}
+
+const char *fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_NULL: return "a required pointer is NULL";
+        case FA_ERR_ALIGN: return "a pointer is not aligned (16 bytes; 4 for lse)";
+        case FA_ERR_SHAPE: return "bad shape: B, H, N must be >= 1 and B*H*ceil(N/256) must fit in int32";
+        case FA_ERR_UNSUPPORTED: return "unsupported head dimension for this element type";
+        case FA_ERR_LAUNCH: return "CUDA launch or tensor-map encoding failed";
+        case FA_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int fa_get_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_LAUNCH;
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_LAUNCH;
+    if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_LAUNCH;
+    return v;
+}
+
+int fa_num_sms(void) {
+    DeviceInfo *di = device_info();
+    return di ? di->num_sms : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"

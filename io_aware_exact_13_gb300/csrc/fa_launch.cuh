@@ -1,0 +1,71 @@
+// fa_launch.cuh -- host-side launch of the forward kernel for one element type.
+// Included by one translation unit per element type; the C ABI in fa_api.cu
+// validates arguments first and then calls launch_fwd<T>().
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct LaunchArgs {
+    const void *q, *k, *v;
+    const float *mask;
+    void *out;
+    float *lse;
+    int B, H, N, d;
+    float scale;
+    int causal;
+    cudaStream_t stream;
+    int *status;      // device status word
+    int num_sms;
+    uint64_t timeout_ns;
+};
+
+// Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with 128-row x
+// 128-byte boxes and 128-byte swizzle. Returns false on failure.
+bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d, int N,
+                     int BH);
+
+template <typename T, int D, bool CAUSAL, bool MASK>
+int launch_variant(const LaunchArgs &a) {
+    using C = Cfg<T, D>;
+    auto kern = fa_fwd_kernel<T, D, CAUSAL, MASK>;
+    // The register split between warpgroups assumes 168 registers per thread at
+    // launch (384 x 168 = 256 x 216 + 128 x 72). Refuse to launch otherwise.
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
+    if (attr.numRegs * kThreads < 256 * 216 + 128 * 72) return -5;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return -5;
+    CUtensorMap tq, tk, tv;
+    const int BH = a.B * a.H;
+    if (!encode_rows_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.N, BH)) return -5;
+    if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BH)) return -5;
+    if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BH)) return -5;
+    FwdParams p;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.mask = a.mask;
+    p.status = a.status;
+    p.B = a.B;
+    p.H = a.H;
+    p.N = a.N;
+    p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
+    p.n_kv = (a.N + kBK - 1) / kBK;
+    p.n_items = BH * p.n_qblk;
+    p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    p.timeout_ns = a.timeout_ns;
+    const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+template <typename T, int D>
+int launch_d(const LaunchArgs &a) {
+    if (a.causal) return a.mask ? launch_variant<T, D, true, true>(a) : launch_variant<T, D, true, false>(a);
+    return a.mask ? launch_variant<T, D, false, true>(a) : launch_variant<T, D, false, false>(a);
+}
+
+}  // namespace fa

@@ -1,0 +1,134 @@
+"""Python binding of the C ABI in ``include/fa.h`` (argument marshalling only).
+
+Every function here forwards device pointers, sizes and the current CUDA
+stream to ``libfa.so``; all arithmetic runs in the library's CUDA kernels.
+There is no CPU fallback: importing this module fails loudly when the library
+has not been built, and every call raises if the library returns an error.
+
+Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
+``fa_status_string``, ``fa_get_device_status``, ``fa_num_sms``. ``attention``
+is a convenience wrapper that allocates O and lse with torch and picks the
+entry point from the input dtype.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it with `python -m io_aware_exact_13_gb300.build` "
+        "(there is no fallback implementation)")
+lib = ctypes.CDLL(_LIB_PATH)
+
+FA_OK = 0
+FA_ERR_NULL = -1
+FA_ERR_ALIGN = -2
+FA_ERR_SHAPE = -3
+FA_ERR_UNSUPPORTED = -4
+FA_ERR_LAUNCH = -5
+FA_ERR_TIMEOUT = -6
+
+# Every symbol the header declares, with its ctypes signature.
+_vp = ctypes.c_void_p
+_FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+             ctypes.c_float, ctypes.c_int, _vp]
+SIGNATURES = {
+    "fa_fwd": (ctypes.c_int, _FWD_ARGS),
+    "fa_fwd_fp16": (ctypes.c_int, _FWD_ARGS),
+    "fa_fwd_fp32": (ctypes.c_int, _FWD_ARGS),
+    "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa_get_device_status": (ctypes.c_int, [_vp]),
+    "fa_num_sms": (ctypes.c_int, []),
+}
+for _name, (_res, _args) in SIGNATURES.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {fa_status_string(status)} (status {status})")
+        self.status = status
+
+
+def fa_status_string(status: int) -> str:
+    return lib.fa_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _raw_fwd(fn_name, q, k, v, mask, out, lse, B, H, N, d, scale, causal, stream):
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), int(B), int(H), int(N),
+                               int(d), float(scale), int(bool(causal)), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def _check(q, k, v, mask, out, lse, dtype):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape or out.shape != q.shape:
+        raise ValueError("q, k, v, out must all be [B, H, N, d]")
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, N] tensor")
+    if mask is not None and (mask.dtype != torch.float32 or not mask.is_cuda or not mask.is_contiguous()
+                             or mask.shape != (B, N, N)):
+        raise ValueError("mask must be a contiguous CUDA float32 [B, N, N] tensor")
+    return B, H, N, d
+
+
+def fa_fwd(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
+    """bf16 forward into caller-provided ``out`` [B,H,N,d] and ``lse`` [B,H,N]."""
+    B, H, N, d = _check(q, k, v, mask_or_null, out, lse, torch.bfloat16)
+    _raw_fwd("fa_fwd", q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_fp16(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
+    """fp16 forward into caller-provided ``out`` and ``lse``."""
+    B, H, N, d = _check(q, k, v, mask_or_null, out, lse, torch.float16)
+    _raw_fwd("fa_fwd_fp16", q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_fp32(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
+    """fp32 (TF32 tensor-core) forward into caller-provided ``out`` and ``lse``."""
+    B, H, N, d = _check(q, k, v, mask_or_null, out, lse, torch.float32)
+    _raw_fwd("fa_fwd_fp32", q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream)
+
+
+_BY_DTYPE = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_fp16, torch.float32: fa_fwd_fp32}
+
+
+def attention(q, k, v, mask=None, scale=None, causal=False, out=None, lse=None, stream=None):
+    """O, lse = softmax(scale * q k^T + mask) v for [B,H,N,d] CUDA tensors."""
+    if q.dtype not in _BY_DTYPE:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
+    return out, lse
+
+
+def fa_get_device_status(stream=None) -> int:
+    return int(lib.fa_get_device_status(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def fa_num_sms() -> int:
+    return int(lib.fa_num_sms())

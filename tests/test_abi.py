@@ -1,0 +1,94 @@
+"""The C-ABI library: it loads, exports every symbol include/fa.h declares, and
+rejects bad arguments on the host before touching the GPU. CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from io_aware_exact_13_gb300 import build
+
+    build.build()
+    from io_aware_exact_13_gb300 import fa as mod
+
+    return mod
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_header_declares_the_forward_family():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_fwd_fp16", "fa_fwd_fp32", "fa_status_string", "fa_get_device_status", "fa_num_sms"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa._LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libfa.so does not export {name}"
+        assert name in fa.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_status_strings(fa):
+    for code in range(0, -7, -1):
+        s = fa.fa_status_string(code)
+        assert s and s != "unknown status"
+    assert fa.fa_status_string(12345) == "unknown status"
+
+
+def _call(fa, name, q=0x10000, k=0x20000, v=0x30000, mask=None, out=0x40000, lse=0x50000, B=1, H=1, N=16, d=128,
+          scale=0.1, causal=0):
+    f = getattr(fa.lib, name)
+    return f(ctypes.c_void_p(q) if q else None, ctypes.c_void_p(k) if k else None,
+             ctypes.c_void_p(v) if v else None, ctypes.c_void_p(mask) if mask else None,
+             ctypes.c_void_p(out) if out else None, ctypes.c_void_p(lse) if lse else None,
+             B, H, N, d, ctypes.c_float(scale), causal, None)
+
+
+@pytest.mark.parametrize("name", ["fa_fwd", "fa_fwd_fp16", "fa_fwd_fp32"])
+def test_host_validation_rejects_before_launch(fa, name):
+    assert _call(fa, name, q=0) == fa.FA_ERR_NULL
+    assert _call(fa, name, lse=0) == fa.FA_ERR_NULL
+    assert _call(fa, name, out=0) == fa.FA_ERR_NULL
+    assert _call(fa, name, k=0x20008) == fa.FA_ERR_ALIGN
+    assert _call(fa, name, mask=0x60004) == fa.FA_ERR_ALIGN
+    assert _call(fa, name, lse=0x50002) == fa.FA_ERR_ALIGN
+    assert _call(fa, name, N=0) == fa.FA_ERR_SHAPE
+    assert _call(fa, name, B=-1) == fa.FA_ERR_SHAPE
+    assert _call(fa, name, H=0) == fa.FA_ERR_SHAPE
+    assert _call(fa, name, B=1 << 16, H=1 << 16) == fa.FA_ERR_SHAPE
+    assert _call(fa, name, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _call(fa, name, d=256) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp32_head_dim_128_is_unsupported(fa):
+    assert _call(fa, "fa_fwd_fp32", d=128) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_binding_checks_shapes_without_a_gpu(fa):
+    import torch
+
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.attention(q, q, q)  # CPU tensors are refused by the binding
+
+
+def test_product_path_does_not_import_the_oracle():
+    """Nothing under the package or bench's GPU path may import oracle/."""
+    pkg = os.path.join(ROOT, "io_aware_exact_13_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", txt, re.M), f
+                assert "attn_oracle" not in txt and "liboracle" not in txt, f
