@@ -48,7 +48,7 @@ typedef enum {
     FA_OK = 0,
     FA_ERR_NULL = -1,        /* a required pointer is NULL */
     FA_ERR_ALIGN = -2,       /* a pointer is not 16-byte aligned */
-    FA_ERR_SHAPE = -3,       /* B, H or N < 1, or a size overflows */
+    FA_ERR_SHAPE = -3,       /* B, H or N < 1, or a size overflows its limit */
     FA_ERR_UNSUPPORTED = -4, /* d not supported for this element type */
     FA_ERR_LAUNCH = -5,      /* the CUDA launch (or tensor-map encoding) failed */
     FA_ERR_TIMEOUT = -6      /* a device-side wait gave up (device status word) */
@@ -62,10 +62,8 @@ int fa_fwd(const void *q, const void *k, const void *v, const float *mask_or_nul
 int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                 float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
 
-/* fp32 Q/K/V/out. Products run on the tensor cores in TF32 (inputs rounded to
- * TF32, fp32 accumulation); P is kept in TF32. d = 64 only (d = 128 returns
- * FA_ERR_UNSUPPORTED: two fp32 query tiles and a K/V ring do not fit in
- * shared memory). */
+/* fp32 Q/K/V/out, computed in fp32 on the CUDA cores (no tensor cores, no
+ * rounding of the inputs). d in {64, 128}; B*H must not exceed 65535. */
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                 float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
 

@@ -81,7 +81,7 @@ int check_args(Type ty, const void *q, const void *k, const void *v, const float
     const int64_t items = bh * ((static_cast<int64_t>(N) + 255) / 256);
     if (items > INT32_MAX) return FA_ERR_SHAPE;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if (ty == Type::FP32 && d != 64) return FA_ERR_UNSUPPORTED;
+    if (ty == Type::FP32 && bh > 65535) return FA_ERR_SHAPE;
     return FA_OK;
 }
 

@@ -33,10 +33,10 @@ int launch_variant(const LaunchArgs &a) {
     using C = Cfg<T, D>;
     auto kern = fa_fwd_kernel<T, D, CAUSAL, MASK>;
     // The register split between warpgroups assumes 168 registers per thread at
-    // launch (384 x 168 = 256 x 216 + 128 x 72). Refuse to launch otherwise.
+    // launch (384 x 168 = 256 x 208 + 128 x 88). Refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
-    if (attr.numRegs * kThreads < 256 * 216 + 128 * 72) return -5;
+    if (attr.numRegs * kThreads < 256 * 208 + 128 * 88) return -5;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return -5;
     CUtensorMap tq, tk, tv;

@@ -106,7 +106,7 @@ def fa_fwd_fp16(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
 
 
 def fa_fwd_fp32(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
-    """fp32 (TF32 tensor-core) forward into caller-provided ``out`` and ``lse``."""
+    """fp32 forward (fp32 arithmetic on the CUDA cores) into caller-provided ``out`` and ``lse``."""
     B, H, N, d = _check(q, k, v, mask_or_null, out, lse, torch.float32)
     _raw_fwd("fa_fwd_fp32", q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream)
 

@@ -71,8 +71,8 @@ def test_host_validation_rejects_before_launch(fa, name):
     assert _call(fa, name, d=256) == fa.FA_ERR_UNSUPPORTED
 
 
-def test_fp32_head_dim_128_is_unsupported(fa):
-    assert _call(fa, "fa_fwd_fp32", d=128) == fa.FA_ERR_UNSUPPORTED
+def test_fp32_grid_limit(fa):
+    assert _call(fa, "fa_fwd_fp32", B=256, H=257) == fa.FA_ERR_SHAPE
 
 
 def test_binding_checks_shapes_without_a_gpu(fa):
