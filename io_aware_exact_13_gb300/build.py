@@ -53,7 +53,7 @@ def _compile(src: str) -> tuple[str, str]:
 
 def check_ptxas_log(log: str) -> tuple[list[str], list[str]]:
     """(errors, warnings) from ptxas -v output. Error: a forward kernel that does
-    not launch with 168 registers per thread (the warpgroup register split is
+    not launch with 128 registers per thread (the warpgroup register split is
     sized for exactly that). Warning: register spills."""
     problems, warnings = [], []
     kernel = None
@@ -65,8 +65,8 @@ def check_ptxas_log(log: str) -> tuple[list[str], list[str]]:
         if m and kernel and (int(m.group(1)) or int(m.group(2))):
             warnings.append(f"{kernel}: spills ({m.group(0)})")
         m = re.search(r"Used (\d+) registers", line)
-        if m and kernel and "fa_fwd_kernel" in kernel and int(m.group(1)) != 168:
-            problems.append(f"{kernel}: uses {m.group(1)} registers, expected 168")
+        if m and kernel and "fa_fwd_kernel" in kernel and int(m.group(1)) != 128:
+            problems.append(f"{kernel}: uses {m.group(1)} registers, expected 128")
     return problems, warnings
 
 

@@ -120,13 +120,13 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
 
 namespace fa {
 bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d, int N,
-                     int BH) {
+                     int BH, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
                              static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

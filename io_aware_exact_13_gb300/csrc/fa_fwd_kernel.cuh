@@ -10,20 +10,29 @@
 // each score tile once it has been folded into (m, l, a). Only O and the
 // per-row log-sum-exp reach global memory.
 //
-// GB300 mapping (one persistent CTA per SM, 12 warps):
+// GB300 mapping (one persistent CTA per SM, 16 warps):
 //   warps 0-3   softmax + epilogue for query tile 0 (thread r owns row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue for query tile 1
-//   warp  8     TMA producer: Q tiles once per work item, then a K/V ring
-//   warp  9     MMA issuer: S = Q K^T and O += P V on tcgen05, fp32
-//               accumulators in tensor memory (TMEM); the warp runs the loop,
-//               lane 0 issues
-//   warps 10-11 idle
-// TMEM (512 columns x 128 lanes x 32 bit):
-//   S_t  columns [128 t, 128 t + 128)       P_t aliases the start of S_t
-//   O_t  columns [256 + 128 t, 256 + 128 t + D)
+//   warp  8     TMA producer: Q tiles once per work item, then K and V rings
+//   warps 9-10  S issuers: S_t = Q_t K^T on tcgen05 for tile t = 0, 1
+//   warps 11-12 PV issuers: O_t += P_t V for tile t = 0, 1
+//   warps 13-15 idle (they complete the last warpgroup)
+// Each issuing warp runs its loop warp-uniformly and lane 0 issues. Four
+// independent issue streams keep the per-wait and per-instruction issue cost
+// (barrier operations compete with MMA operand reads for shared memory) off
+// the tensor core's critical path; accumulators are fp32 in tensor memory.
 // A work item is (batch*head, 256 query rows) = two 128-row query tiles that
 // share every K/V tile; items are visited longest-first (causal rows near the
 // end of the sequence see the most keys).
+//
+// K/V blocks are 64 keys, so that tensor memory (512 columns x 128 lanes x 32
+// bit) holds, without aliasing,
+//   S_t      columns [64 t, 64 t + 64)                 (fp32 scores, one block)
+//   P_t,b    columns [128 + 64 t + 32 b, ... + 32)     (16-bit P, two buffers)
+//   O_t      columns [256 + 128 t, 256 + 128 t + D)    (fp32 accumulator)
+// The softmax warps copy S_t(j) to registers and release it at once, so the MMA
+// for S_t(j+1) runs while they compute P_t(j); with P double-buffered the only
+// ordering left between the softmax and the tensor core is the data itself.
 //
 // Scores are handled in the base-2 domain: x = s * scale * log2(e) (+ M * log2(e)),
 // p = 2^(x - m_ref). The reference maximum m_ref is only moved when the block
@@ -44,9 +53,9 @@
 namespace fa {
 
 constexpr int kBQ = 128;           // rows per query tile (= TMEM lanes)
-constexpr int kBK = 128;           // keys per K/V tile
+constexpr int kBK = 64;            // keys per K/V block
 constexpr int kRowsPerItem = 256;  // two query tiles per work item
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr float kTau = 8.0f;       // lazy-rescale threshold, log2 units
 constexpr int kStatusTimeout = -6; // value written to the device status word
 
@@ -66,25 +75,32 @@ struct Elem<__half> {
 template <typename T, int D>
 struct Cfg {
     static constexpr int EB = sizeof(T);
-    static constexpr int ROW_BYTES = D * EB;               // one row of Q/K/V
-    static constexpr int CHUNK_ELEMS = 128 / EB;           // elements per 128-byte swizzle row
-    static constexpr int NCH = ROW_BYTES / 128;            // swizzle chunks per row
-    static constexpr int CHUNK_BYTES = 128 * 128;          // 128 rows x 128 bytes
-    static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;   // one 128-row tile
-    static constexpr int STAGES = (TILE_BYTES <= 16384) ? 8 : 5;
-    static constexpr int KSTEPS_S = ROW_BYTES / 32;        // 32 bytes of K per MMA instruction
-    static constexpr int P_COLS = 64;                      // TMEM columns holding P (two 16-bit values each)
-    static constexpr int KSTEPS_PV = P_COLS / 8;           // 8 TMEM columns of P per MMA instruction
-    static constexpr int V_KSTEP_BYTES = (32 / EB) * 128;  // keys per instruction x 128 bytes per key row
+    static constexpr int ROW_BYTES = D * EB;                // one row of Q/K/V
+    static constexpr int CHUNK_ELEMS = 128 / EB;            // elements per 128-byte swizzle row
+    static constexpr int NCH = ROW_BYTES / 128;             // swizzle chunks per row
+    static constexpr int Q_CHUNK = kBQ * 128;               // 128 rows x 128 bytes
+    static constexpr int KV_CHUNK = kBK * 128;              // 64 rows x 128 bytes
+    static constexpr int Q_TILE = NCH * Q_CHUNK;            // one 128-row query tile
+    static constexpr int KV_TILE = NCH * KV_CHUNK;          // one 64-key K or V block
+    static constexpr int KSTEPS_S = ROW_BYTES / 32;         // 32 bytes of the head dim per MMA
+    static constexpr int KSTEPS_PV = kBK / 16;              // 16 keys per MMA
+    static constexpr int V_KSTEP_BYTES = 16 * 128;          // 16 key rows x 128 bytes
     static constexpr uint32_t IDESC_S = make_idesc(Elem<T>::fmt, 128, kBK, 0);
     static constexpr uint32_t IDESC_PV = make_idesc(Elem<T>::fmt, 128, D, 1);
-    // shared memory: Q0 Q1 | K/V ring | barriers
+    // shared memory: Q0 Q1 | K ring | V ring | barriers
     static constexpr int SMEM_Q = 0;
-    static constexpr int SMEM_KV = 2 * TILE_BYTES;
-    static constexpr int SMEM_BAR = SMEM_KV + STAGES * TILE_BYTES;
-    static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 + 2 + 2 + 1;
+    static constexpr int SMEM_KV = 2 * Q_TILE;
+    static constexpr int RING_FREE = 232448 - 1024 - 512 - SMEM_KV;
+    static constexpr int RING = (RING_FREE / KV_TILE / 2) > 6 ? 6 : (RING_FREE / KV_TILE / 2);  // slots per ring
+    static constexpr int STAGES = 2 * RING;
+    static constexpr int SMEM_V = SMEM_KV + RING * KV_TILE;
+    static constexpr int SMEM_BAR = SMEM_KV + STAGES * KV_TILE;
+    // q_full[2] q_empty[2] k_full[R] k_empty[R] v_full[R] v_empty[R] s_full[2] s_free[2] p_full[2][2]
+    // pv_done[2][2] drain
+    static constexpr int NUM_BARS = 2 + 2 + 4 * RING + 2 + 2 + 4 + 4 + 1;
     static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
     static_assert(NCH >= 1 && ROW_BYTES % 128 == 0, "row must be a whole number of 128-byte swizzle rows");
+    static_assert(RING >= 2, "K/V rings too small");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -96,7 +112,7 @@ struct FwdParams {
     int B, H, N;
     int n_items;        // B * H * ceil(N / 256)
     int n_qblk;         // ceil(N / 256)
-    int n_kv;           // ceil(N / 128)
+    int n_kv;           // ceil(N / 64)
     float scale_log2;   // scale * log2(e)
     uint64_t timeout_ns;
 };
@@ -121,7 +137,7 @@ __device__ __forceinline__ void item_coords(const FwdParams &p, int item, int &b
     q0 = qb * kRowsPerItem;
 }
 
-// Number of K/V tiles query tile t of an item at q0 must visit.
+// Number of K/V blocks query tile t of an item at q0 must visit.
 template <bool CAUSAL>
 __device__ __forceinline__ int tile_nkv(const FwdParams &p, int q0, int t) {
     const int r0 = q0 + t * kBQ;
@@ -131,16 +147,23 @@ __device__ __forceinline__ int tile_nkv(const FwdParams &p, int q0, int t) {
     return last_row / kBK + 1;
 }
 
+template <int R>
 struct Sync {
     uint64_t *bars;
-    __device__ __forceinline__ uint32_t q_full(int t) const { return smem_u32(bars + t); }
-    __device__ __forceinline__ uint32_t q_empty(int t) const { return smem_u32(bars + 2 + t); }
-    __device__ __forceinline__ uint32_t kv_full(int s) const { return smem_u32(bars + 4 + s); }
-    __device__ __forceinline__ uint32_t kv_empty(int s, int stages) const { return smem_u32(bars + 4 + stages + s); }
-    __device__ __forceinline__ uint32_t s_full(int t, int stages) const { return smem_u32(bars + 4 + 2 * stages + t); }
-    __device__ __forceinline__ uint32_t p_full(int t, int stages) const { return smem_u32(bars + 6 + 2 * stages + t); }
-    __device__ __forceinline__ uint32_t o_full(int t, int stages) const { return smem_u32(bars + 8 + 2 * stages + t); }
-    __device__ __forceinline__ uint32_t drain(int stages) const { return smem_u32(bars + 10 + 2 * stages); }
+    __device__ __forceinline__ uint32_t at(int i) const { return smem_u32(bars + i); }
+    __device__ __forceinline__ uint32_t q_full(int t) const { return at(t); }
+    __device__ __forceinline__ uint32_t q_empty(int t) const { return at(2 + t); }
+    __device__ __forceinline__ uint32_t k_full(int s) const { return at(4 + s); }
+    __device__ __forceinline__ uint32_t k_empty(int s) const { return at(4 + R + s); }
+    __device__ __forceinline__ uint32_t v_full(int s) const { return at(4 + 2 * R + s); }
+    __device__ __forceinline__ uint32_t v_empty(int s) const { return at(4 + 3 * R + s); }
+    __device__ __forceinline__ uint32_t s_full(int t) const { return at(4 + 4 * R + t); }
+    __device__ __forceinline__ uint32_t s_free(int t) const { return at(6 + 4 * R + t); }
+    // One P-ready and one P-consumed barrier per (tile, P buffer): each can then
+    // run at most one phase ahead of its waiter, which the parity waits need.
+    __device__ __forceinline__ uint32_t p_full(int t, int b) const { return at(8 + 4 * R + 2 * t + b); }
+    __device__ __forceinline__ uint32_t pv_done(int t, int b) const { return at(12 + 4 * R + 2 * t + b); }
+    __device__ __forceinline__ uint32_t drain() const { return at(16 + 4 * R); }
 };
 
 // Bounded wait: returns false (after recording a timeout and raising the CTA's
@@ -163,6 +186,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// Warp-uniform bounded wait (every lane waits; all lanes agree on the result).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          const FwdParams &p) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, p));
+}
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <>
@@ -181,10 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using C = Cfg<T, D>;
-    constexpr int ST = C::STAGES;
+    constexpr int R = C::RING;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Sync sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};
+    Sync<R> sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -195,15 +224,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(sy.q_full(t), 1);
             mbar_init(sy.q_empty(t), 1);
-            mbar_init(sy.s_full(t, ST), 1);
-            mbar_init(sy.p_full(t, ST), kBQ);
-            mbar_init(sy.o_full(t, ST), 1);
+            mbar_init(sy.s_full(t), 1);
+            mbar_init(sy.s_free(t), kBQ);
+            mbar_init(sy.p_full(t, 0), kBQ);
+            mbar_init(sy.p_full(t, 1), kBQ);
+            mbar_init(sy.pv_done(t, 0), 1);
+            mbar_init(sy.pv_done(t, 1), 1);
         }
-        for (int s = 0; s < ST; ++s) {
-            mbar_init(sy.kv_full(s), 1);
-            mbar_init(sy.kv_empty(s, ST), 1);
+        for (int s = 0; s < R; ++s) {  // a K or V slot is released by both tiles' issuers
+            mbar_init(sy.k_full(s), 1);
+            mbar_init(sy.k_empty(s), 2);
+            mbar_init(sy.v_full(s), 1);
+            mbar_init(sy.v_empty(s), 2);
         }
-        mbar_init(sy.drain(ST), 1);
+        mbar_init(sy.drain(), 4);  // one commit per issuing warp
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -223,54 +257,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
     if (warp >= 8) {
-        setmaxnreg_dec<88>();
+        setmaxnreg_dec<56>();
         if (warp == 8) {
             // ---------------------------------------------------------- TMA producer
             // The whole warp runs the (uniform) loop; lane 0 issues the copies.
+            // Load order per item: K_0, then K_{j+1}, V_j for j = 0 .. nmax-1.
             const bool leader = lane == 0;
             const uint64_t pol_kv = policy_evict_last();
             const uint64_t pol_q = policy_evict_first();
             uint32_t qcount[2] = {0, 0};
-            uint32_t kvpos = 0;
+            uint32_t kpos = 0, vpos = 0;
+            int cur_bh = 0;
             bool ok = true;
+            auto load_kv = [&](bool is_v, int blk) -> bool {
+                uint32_t &pos = is_v ? vpos : kpos;
+                const int s = pos % R;
+                const uint32_t full = is_v ? sy.v_full(s) : sy.k_full(s);
+                const uint32_t empty = is_v ? sy.v_empty(s) : sy.k_empty(s);
+                if (!wait_warp(empty, ((pos / R) & 1u) ^ 1u, abort_flag, p)) return false;
+                if (leader) {
+                    const uint32_t dst = smem_u32(smem + (is_v ? C::SMEM_V : C::SMEM_KV) + s * C::KV_TILE);
+                    mbar_arrive_expect_tx(full, C::KV_TILE);
+#pragma unroll
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_3d(dst + c * C::KV_CHUNK, is_v ? &tm_v : &tm_k, full, c * C::CHUNK_ELEMS, blk * kBK,
+                                    cur_bh, pol_kv);
+                }
+                __syncwarp();
+                ++pos;
+                return true;
+            };
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                int bh, q0;
-                item_coords(p, item, bh, q0);
+                int q0;
+                item_coords(p, item, cur_bh, q0);
                 const int n0 = tile_nkv<CAUSAL>(p, q0, 0), n1 = tile_nkv<CAUSAL>(p, q0, 1);
                 const int nmax = max(n0, n1);
                 for (int t = 0; t < 2 && ok; ++t) {
                     if ((t == 0 ? n0 : n1) == 0) continue;
-                    ok = __all_sync(0xffffffffu, wait_bounded(sy.q_empty(t), (qcount[t] & 1u) ^ 1u, abort_flag, p));
+                    ok = wait_warp(sy.q_empty(t), (qcount[t] & 1u) ^ 1u, abort_flag, p);
                     if (!ok) break;
                     if (leader) {
-                        const uint32_t dst = smem_u32(smem + C::SMEM_Q + t * C::TILE_BYTES);
-                        mbar_arrive_expect_tx(sy.q_full(t), C::TILE_BYTES);
+                        const uint32_t dst = smem_u32(smem + C::SMEM_Q + t * C::Q_TILE);
+                        mbar_arrive_expect_tx(sy.q_full(t), C::Q_TILE);
 #pragma unroll
                         for (int c = 0; c < C::NCH; ++c)
-                            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, sy.q_full(t), c * C::CHUNK_ELEMS,
-                                        q0 + t * kBQ, bh, pol_q);
+                            tma_load_3d(dst + c * C::Q_CHUNK, &tm_q, sy.q_full(t), c * C::CHUNK_ELEMS, q0 + t * kBQ,
+                                        cur_bh, pol_q);
                     }
                     __syncwarp();
                     ++qcount[t];
                 }
+                if (ok) ok = load_kv(false, 0);
                 for (int j = 0; ok && j < nmax; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
-                        const int s = kvpos % ST;
-                        const uint32_t ph = (kvpos / ST) & 1u;
-                        ok = __all_sync(0xffffffffu, wait_bounded(sy.kv_empty(s, ST), ph ^ 1u, abort_flag, p));
-                        if (!ok) break;
-                        if (leader) {
-                            const uint32_t dst = smem_u32(smem + C::SMEM_KV + s * C::TILE_BYTES);
-                            mbar_arrive_expect_tx(sy.kv_full(s), C::TILE_BYTES);
-                            const CUtensorMap *m = kv == 0 ? &tm_k : &tm_v;
-#pragma unroll
-                            for (int c = 0; c < C::NCH; ++c)
-                                tma_load_3d(dst + c * C::CHUNK_BYTES, m, sy.kv_full(s), c * C::CHUNK_ELEMS, j * kBK,
-                                            bh, pol_kv);
-                        }
-                        __syncwarp();
-                        ++kvpos;
-                    }
+                    if (j + 1 < nmax) ok = load_kv(false, j + 1);
+                    if (ok) ok = load_kv(true, j);
                 }
             }
             if (!ok && leader) {  // let every copy in flight land before the CTA can exit
@@ -280,109 +320,119 @@ __global__ void __launch_bounds__(kThreads, 1)
                         while (!mbar_try_wait(sy.q_full(t), (qcount[t] - 1) & 1u) &&
                                global_timer_ns() - t0 < p.timeout_ns) {
                         }
-                // the most recent load of each ring slot is positions kvpos-ST .. kvpos-1
-                for (uint32_t pos = kvpos > (uint32_t)ST ? kvpos - ST : 0; pos < kvpos; ++pos)
-                    while (!mbar_try_wait(sy.kv_full(pos % ST), (pos / ST) & 1u) &&
-                           global_timer_ns() - t0 < p.timeout_ns) {
+                // the most recent load of each slot is positions pos-R .. pos-1
+                for (uint32_t q = kpos > (uint32_t)R ? kpos - R : 0; q < kpos; ++q)
+                    while (!mbar_try_wait(sy.k_full(q % R), (q / R) & 1u) && global_timer_ns() - t0 < p.timeout_ns) {
+                    }
+                for (uint32_t q = vpos > (uint32_t)R ? vpos - R : 0; q < vpos; ++q)
+                    while (!mbar_try_wait(sy.v_full(q % R), (q / R) & 1u) && global_timer_ns() - t0 < p.timeout_ns) {
                     }
             }
-        } else if (warp == 9) {
-            // ---------------------------------------------------------- MMA issuer
-            // Whole warp, uniform control flow; lane 0 issues every MMA and every
-            // commit. Descriptors are built once and advanced by constant
-            // offsets (in 16-byte units).
+        } else if (warp == 9 || warp == 10) {
+            // ---------------------------------------------------------- S issuer for tile t
+            // S_t(j) = Q_t K_j^T into S_t's columns, after the softmax has copied the
+            // previous S_t out. K slots this tile does not need are released at once.
+            const int t = warp - 9;
             const uint32_t issue = lane == 0 ? 1u : 0u;
-            uint32_t qcount[2] = {0, 0}, pcount[2] = {0, 0};
-            uint32_t kvpos = 0;
-            const uint32_t q_base = smem_u32(smem + C::SMEM_Q);
-            const uint32_t kv_base = smem_u32(smem + C::SMEM_KV);
-            const uint64_t dq = smem_desc_sw128(q_base, 16, 1024);               // Q tile 0, K-major
-            const uint64_t dk = smem_desc_sw128(kv_base, 16, 1024);              // ring slot 0 as K (K-major)
-            const uint64_t dv = smem_desc_sw128(kv_base, C::CHUNK_BYTES, 1024);  // ring slot 0 as V (N-major)
-            constexpr uint64_t TILE16 = C::TILE_BYTES >> 4;
+            const uint64_t a0 = smem_desc_sw128(smem_u32(smem + C::SMEM_Q + t * C::Q_TILE), 16, 1024);
+            const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + C::SMEM_KV), 16, 1024);
+            const uint32_t d_s = tmem + t * 64;
+            constexpr uint64_t KVT16 = C::KV_TILE >> 4;
+            uint32_t qcount = 0, s_issued = 0, kpos = 0;
             bool ok = true;
-            auto s_mma = [&](int t, int slot) {  // S_t = Q_t K^T
-                const uint64_t a0 = dq + t * TILE16, b0 = dk + slot * TILE16;
-#pragma unroll
-                for (int k = 0; k < C::KSTEPS_S; ++k) {
-                    const uint64_t off = (uint64_t)(((k / 4) * C::CHUNK_BYTES + (k % 4) * 32) >> 4);
-                    mma_ss(tmem + t * 128, a0 + off, b0 + off, C::IDESC_S, k > 0 ? 1u : 0u, issue);
-                }
-            };
-            auto pv_mma = [&](int t, int slot, uint32_t acc) {  // O_t (+)= P_t V
-                const uint64_t b0 = dv + slot * TILE16;
-#pragma unroll
-                for (int k = 0; k < C::KSTEPS_PV; ++k)
-                    mma_ts(tmem + 256 + t * 128, tmem + t * 128 + k * 8,
-                           b0 + (uint64_t)((k * C::V_KSTEP_BYTES) >> 4), C::IDESC_PV, k > 0 ? 1u : acc, issue);
-            };
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
                 int bh, q0;
                 item_coords(p, item, bh, q0);
-                const int n[2] = {tile_nkv<CAUSAL>(p, q0, 0), tile_nkv<CAUSAL>(p, q0, 1)};
-                const int nmax = max(n[0], n[1]);
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (n[t] == 0) continue;
-                    ok = __all_sync(0xffffffffu, wait_bounded(sy.q_full(t), qcount[t] & 1u, abort_flag, p));
-                    ++qcount[t];
+                const int nt = tile_nkv<CAUSAL>(p, q0, t);
+                const int nmax = max(tile_nkv<CAUSAL>(p, q0, 0), tile_nkv<CAUSAL>(p, q0, 1));
+                if (nt > 0) {
+                    ok = wait_warp(sy.q_full(t), qcount & 1u, abort_flag, p);
+                    ++qcount;
                 }
-                if (!ok) break;
-                int slot_v = 0;  // slot of V_{j-1}
-                for (int j = 0; j <= nmax && ok; ++j) {
-                    int slot_k = 0;
-                    if (j > 0) {  // V_{j-1}
-                        slot_v = kvpos % ST;
-                        ok = __all_sync(0xffffffffu,
-                                        wait_bounded(sy.kv_full(slot_v), (kvpos / ST) & 1u, abort_flag, p));
-                        ++kvpos;
-                        if (!ok) break;
-                    }
-                    if (j < nmax) {  // K_j
-                        slot_k = kvpos % ST;
-                        ok = __all_sync(0xffffffffu,
-                                        wait_bounded(sy.kv_full(slot_k), (kvpos / ST) & 1u, abort_flag, p));
-                        ++kvpos;
-                        if (!ok) break;
-                    }
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (j > 0 && j - 1 < n[t]) {
-                            ok = __all_sync(0xffffffffu,
-                                            wait_bounded(sy.p_full(t, ST), pcount[t] & 1u, abort_flag, p));
-                            ++pcount[t];
-                            if (!ok) break;
-                            tc_fence_after();
-                            pv_mma(t, slot_v, j - 1 > 0 ? 1u : 0u);
-                            tc_commit(sy.o_full(t, ST), issue);
-                        }
-                        if (j < n[t]) {
-                            s_mma(t, slot_k);
-                            tc_commit(sy.s_full(t, ST), issue);
-                            if (j == n[t] - 1) tc_commit(sy.q_empty(t), issue);
-                        }
-                    }
+                for (int j = 0; ok && j < nmax; ++j, ++kpos) {
+                    const int slot = kpos % R;
+                    ok = wait_warp(sy.k_full(slot), (kpos / R) & 1u, abort_flag, p);
                     if (!ok) break;
-                    if (j > 0) tc_commit(sy.kv_empty(slot_v, ST), issue);
-                    if (j < nmax) tc_commit(sy.kv_empty(slot_k, ST), issue);
+                    if (j >= nt) {
+                        if (lane == 0) mbar_arrive(sy.k_empty(slot));
+                        continue;
+                    }
+                    if (s_issued > 0) ok = wait_warp(sy.s_free(t), (s_issued - 1) & 1u, abort_flag, p);
+                    if (!ok) break;
+                    ++s_issued;
+                    tc_fence_after();
+                    const uint64_t b0 = kd0 + slot * KVT16;
+#pragma unroll
+                    for (int k = 0; k < C::KSTEPS_S; ++k) {
+                        const uint64_t aoff = (uint64_t)(((k / 4) * C::Q_CHUNK + (k % 4) * 32) >> 4);
+                        const uint64_t boff = (uint64_t)(((k / 4) * C::KV_CHUNK + (k % 4) * 32) >> 4);
+                        mma_ss(d_s, a0 + aoff, b0 + boff, C::IDESC_S, k > 0 ? 1u : 0u, issue);
+                    }
+                    tc_commit(sy.s_full(t), issue);
+                    if (j == nt - 1) tc_commit(sy.q_empty(t), issue);
+                    tc_commit(sy.k_empty(slot), issue);
                 }
             }
-            // every MMA lane 0 issued must be complete before TMEM is released
             __syncwarp();
-            tc_commit(sy.drain(ST), issue);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(sy.drain(ST), 0) && global_timer_ns() - t0 < p.timeout_ns) {
+            tc_commit(sy.drain(), issue);
+        } else if (warp == 11 || warp == 12) {
+            // ---------------------------------------------------------- PV issuer for tile t
+            // O_t (+)= P_t(j) V_j once the softmax has written P_t(j) into buffer g & 1.
+            const int t = warp - 11;
+            const uint32_t issue = lane == 0 ? 1u : 0u;
+            const uint64_t vd0 = smem_desc_sw128(smem_u32(smem + C::SMEM_V), C::KV_CHUNK, 1024);
+            const uint32_t d_o = tmem + 256 + t * 128;
+            const uint32_t a_p = tmem + 128 + t * 64;
+            constexpr uint64_t KVT16 = C::KV_TILE >> 4;
+            uint32_t g = 0, vpos = 0;
+            bool ok = true;
+            for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
+                int bh, q0;
+                item_coords(p, item, bh, q0);
+                const int nt = tile_nkv<CAUSAL>(p, q0, t);
+                const int nmax = max(tile_nkv<CAUSAL>(p, q0, 0), tile_nkv<CAUSAL>(p, q0, 1));
+                for (int j = 0; ok && j < nmax; ++j, ++vpos) {
+                    const int slot = vpos % R;
+                    ok = wait_warp(sy.v_full(slot), (vpos / R) & 1u, abort_flag, p);
+                    if (!ok) break;
+                    if (j >= nt) {
+                        if (lane == 0) mbar_arrive(sy.v_empty(slot));
+                        continue;
+                    }
+                    const uint32_t b = g & 1u;
+                    ok = wait_warp(sy.p_full(t, b), (g >> 1) & 1u, abort_flag, p);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t b0 = vd0 + slot * KVT16;
+#pragma unroll
+                    for (int k = 0; k < C::KSTEPS_PV; ++k)
+                        mma_ts(d_o, a_p + b * 32 + k * 8, b0 + (uint64_t)((k * C::V_KSTEP_BYTES) >> 4), C::IDESC_PV,
+                               (k > 0 || j > 0) ? 1u : 0u, issue);
+                    tc_commit(sy.pv_done(t, b), issue);
+                    tc_commit(sy.v_empty(slot), issue);
+                    ++g;
+                }
             }
+            __syncwarp();
+            tc_commit(sy.drain(), issue);
         }
     } else {
-        setmaxnreg_inc<208>();
+        setmaxnreg_inc<200>();
         // -------------------------------------------------------------- softmax + epilogue
         const int t = warp >> 2;                   // query tile of this warpgroup
         const int r = threadIdx.x & 127;           // row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + t * 128;
+        const uint32_t s_addr = tmem + lane_base + t * 64;
+        const uint32_t p_addr = tmem + lane_base + 128 + t * 64;
         const uint32_t o_addr = tmem + lane_base + 256 + t * 128;
         const float scale_log2 = p.scale_log2;
-        uint32_t scount = 0, ocount = 0;
+        const bool fast = !HAS_MASK && scale_log2 > 0.0f;
+        // x holds raw scores, scaled by sl2 inside the exponent, on the fast path
+        // (no mask, positive scale); otherwise pre-scaled scores with sl2 = 1 (a
+        // -inf raw score times a non-positive scale is not -inf).
+        const float sl2 = fast ? scale_log2 : 1.0f;
+        uint32_t scount = 0;  // S blocks consumed (all items)
+        uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
         bool ok = true;
         for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
             int bh, q0;
@@ -392,57 +442,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = q0 + t * kBQ + r;  // global query row (may be >= N in a ragged tail)
             const int b = bh / p.H;
             float m_ref = -INFINITY, l = 0.0f;
-            for (int j = 0; j < nt; ++j) {
-                ok = __all_sync(0xffffffffu, wait_bounded(sy.s_full(t, ST), scount & 1u, abort_flag, p));
+            for (int j = 0; j < nt; ++j, ++g) {
+                ok = wait_warp(sy.s_full(t), scount & 1u, abort_flag, p);
                 ++scount;
                 if (!ok) break;
                 tc_fence_after();
-                float x[128];
+                uint32_t sr[64];
+                tmem_ld64_nowait(s_addr, sr);
+                tmem_wait_ld_dep64(sr);
+                tc_fence_before();
+                mbar_arrive(sy.s_free(t));  // S_t may now be overwritten by the next block
+                float x[64];
                 const int kbase = j * kBK;
-                // sl2 multiplies x inside the exponent: raw scores with sl2 = scale*log2(e)
-                // on the fast path (no mask, positive scale), pre-scaled scores with sl2 = 1
-                // otherwise (a -inf raw score times a non-positive scale is not -inf).
-                float sl2 = 1.0f;
                 if constexpr (HAS_MASK) {
-                    // 32 columns at a time so that S and mask values are not all live at once
                     const bool row_ok = row < p.N;
                     const float *mrow = p.mask + ((size_t)b * p.N + (size_t)(row_ok ? row : 0)) * p.N + kbase;
                     const bool vec = row_ok && ((p.N & 3) == 0) && (kbase + kBK <= p.N);
+                    if (vec) {
 #pragma unroll
-                    for (int c0 = 0; c0 < 128; c0 += 32) {
-                        uint32_t sr[32];
-                        tmem_ld32_wait(s_addr + c0, sr);
-                        if (vec) {
+                        for (int c = 0; c < 64; c += 4) {
+                            const float4 mv = ld_global_nc_v4(mrow + c);
+                            x[c + 0] = fmaf(__uint_as_float(sr[c + 0]), scale_log2, mv.x * 1.4426950408889634f);
+                            x[c + 1] = fmaf(__uint_as_float(sr[c + 1]), scale_log2, mv.y * 1.4426950408889634f);
+                            x[c + 2] = fmaf(__uint_as_float(sr[c + 2]), scale_log2, mv.z * 1.4426950408889634f);
+                            x[c + 3] = fmaf(__uint_as_float(sr[c + 3]), scale_log2, mv.w * 1.4426950408889634f);
+                        }
+                    } else {
 #pragma unroll
-                            for (int c = 0; c < 32; c += 4) {
-                                const float4 mv = ld_global_nc_v4(mrow + c0 + c);
-                                x[c0 + c + 0] = fmaf(__uint_as_float(sr[c + 0]), scale_log2, mv.x * 1.4426950408889634f);
-                                x[c0 + c + 1] = fmaf(__uint_as_float(sr[c + 1]), scale_log2, mv.y * 1.4426950408889634f);
-                                x[c0 + c + 2] = fmaf(__uint_as_float(sr[c + 2]), scale_log2, mv.z * 1.4426950408889634f);
-                                x[c0 + c + 3] = fmaf(__uint_as_float(sr[c + 3]), scale_log2, mv.w * 1.4426950408889634f);
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) {
-                                const float mv = (row_ok && kbase + c0 + c < p.N) ? __ldg(mrow + c0 + c) : 0.0f;
-                                x[c0 + c] = fmaf(__uint_as_float(sr[c]), scale_log2, mv * 1.4426950408889634f);
-                            }
+                        for (int c = 0; c < 64; ++c) {
+                            const float mv = (row_ok && kbase + c < p.N) ? __ldg(mrow + c) : 0.0f;
+                            x[c] = fmaf(__uint_as_float(sr[c]), scale_log2, mv * 1.4426950408889634f);
                         }
                     }
+                } else if (fast) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]);
                 } else {
-                    // two 64-column halves: the second load is in flight while the first is converted
-                    uint32_t sa[64], sb[64];
-                    tmem_ld64_nowait(s_addr, sa);
-                    tmem_wait_ld_dep64(sa);
-                    tmem_ld64_nowait(s_addr + 64, sb);
-                    const bool fast = scale_log2 > 0.0f;
-                    sl2 = fast ? scale_log2 : 1.0f;
-                    const float pre = fast ? 1.0f : scale_log2;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sa[c]) * pre;
-                    tmem_wait_ld_dep64(sb);
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) x[64 + c] = __uint_as_float(sb[c]) * pre;
+                    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c]) * scale_log2;
                 }
                 // keys past the end of the sequence, and (causal) keys after the query
                 const int tile_row0 = q0 + t * kBQ;
@@ -452,18 +489,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int lim = p.N - 1 - kbase;
                     if (CAUSAL) lim = min(lim, row - kbase);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
+                    for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
                 }
                 // row maximum: eight independent three-input chains, then a short tree
                 float m8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = x[i];
+                for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-                for (int c = 8; c < 120; c += 16)
+                for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[24 + i], x[32 + i]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
+                for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[40 + i], x[48 + i]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
+                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[56 + i]);
                 const float mraw =
                     fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                 const float mb = mraw * sl2;  // sl2 > 0, so scaling commutes with the maximum
@@ -473,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;  // 2^-inf = 0
                 if (__any_sync(0xffffffffu, need) && j > 0) {
                     // O holds P V for blocks < j: wait for the product of block j-1, then scale rows in place
-                    ok = __all_sync(0xffffffffu,
-                                    wait_bounded(sy.o_full(t, ST), (ocount + j - 1) & 1u, abort_flag, p));
+                    const uint32_t gp = g - 1;
+                    ok = wait_warp(sy.pv_done(t, gp & 1u), (gp >> 1) & 1u, abort_flag, p);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -492,27 +529,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref;
                 float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                uint32_t pv[32];
 #pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 64) {
-                    uint32_t pv[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float e0 = ex2_approx(fmaf(x[c0 + 2 * c], sl2, neg));
-                        const float e1 = ex2_approx(fmaf(x[c0 + 2 * c + 1], sl2, neg));
-                        ls[c & 3] += e0 + e1;
-                        pv[c] = pack2<T>(e0, e1);
-                    }
-                    tmem_st32(s_addr + c0 / 2, pv);
+                for (int c = 0; c < 32; ++c) {
+                    const float e0 = ex2_approx(fmaf(x[2 * c], sl2, neg));
+                    const float e1 = ex2_approx(fmaf(x[2 * c + 1], sl2, neg));
+                    ls[c & 3] += e0 + e1;
+                    pv[c] = pack2<T>(e0, e1);
                 }
                 l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                // P buffer (g & 1) was last read by the product of block g - 2
+                if (g >= 2) {
+                    ok = wait_warp(sy.pv_done(t, g & 1u), ((g - 2) >> 1) & 1u, abort_flag, p);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                tmem_st32(p_addr + (g & 1u) * 32, pv);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(sy.p_full(t, ST));
+                mbar_arrive(sy.p_full(t, g & 1u));
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
-            ok = __all_sync(0xffffffffu, wait_bounded(sy.o_full(t, ST), (ocount + nt - 1) & 1u, abort_flag, p));
-            ocount += nt;
+            const uint32_t gl = g - 1;  // the last product of this item
+            ok = wait_warp(sy.pv_done(t, gl & 1u), (gl >> 1) & 1u, abort_flag, p);
             if (!ok) break;
             tc_fence_after();
             const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
@@ -541,6 +581,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 9) {
+        // every MMA of the four issuing warps must be complete before TMEM is released
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(sy.drain(), 0) && global_timer_ns() - t0 < p.timeout_ns) {
+        }
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

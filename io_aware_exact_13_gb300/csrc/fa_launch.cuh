@@ -23,27 +23,27 @@ struct LaunchArgs {
     uint64_t timeout_ns;
 };
 
-// Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with 128-row x
+// Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with box_rows-row x
 // 128-byte boxes and 128-byte swizzle. Returns false on failure.
 bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d, int N,
-                     int BH);
+                     int BH, int box_rows);
 
 template <typename T, int D, bool CAUSAL, bool MASK>
 int launch_variant(const LaunchArgs &a) {
     using C = Cfg<T, D>;
     auto kern = fa_fwd_kernel<T, D, CAUSAL, MASK>;
-    // The register split between warpgroups assumes 168 registers per thread at
-    // launch (384 x 168 = 256 x 208 + 128 x 88). Refuse to launch otherwise.
+    // The register split between warpgroups assumes 128 registers per thread at
+    // launch (512 x 128 = 256 x 200 + 256 x 56). Refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
-    if (attr.numRegs * kThreads < 256 * 208 + 128 * 88) return -5;
+    if (attr.numRegs * kThreads < 256 * 200 + 256 * 56) return -5;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return -5;
     CUtensorMap tq, tk, tv;
     const int BH = a.B * a.H;
-    if (!encode_rows_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.N, BH)) return -5;
-    if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BH)) return -5;
-    if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BH)) return -5;
+    if (!encode_rows_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.N, BH, kBQ)) return -5;
+    if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BH, kBK)) return -5;
+    if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BH, kBK)) return -5;
     FwdParams p;
     p.out = a.out;
     p.lse = a.lse;
