@@ -1,0 +1,194 @@
+"""CPU model of the forward kernel's mbarrier protocol, for one CTA.
+
+Every role of the kernel is a generator that yields the barrier waits and
+arrivals it performs, in the kernel's order: the TMA producer, the two S
+issuers, the two PV issuers and the softmax warps of both query tiles. A
+random scheduler interleaves them with an in-order tensor pipe (commits fire
+when they reach its head) and out-of-order TMA completions.
+
+A barrier here counts completed phases. Waits name the completion they need;
+the kernel passes only its parity, which is exact only while the barrier is
+at most one phase past the awaited completion. ``Bar.done`` asserts exactly
+that, so a protocol that lets a barrier run two phases ahead of a waiter
+fails here even when the interleaving happens not to deadlock.
+
+This models the kernel's synchronisation only (no data). Causal block counts
+follow the kernel: 128-row query tiles, two per work item, 64-key blocks.
+"""
+import random
+
+BQ, BK, ROWS = 128, 64, 256
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.phase = name, count, count, 0
+
+    def arrive(self, n=1):
+        self.pending -= n
+        assert self.pending >= 0, f"{self.name}: more arrivals than the phase expects"
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def done(self, index):
+        assert index < 0 or self.phase <= index + 1, (
+            f"{self.name}: waiting for completion {index} while the barrier is at phase {self.phase} "
+            "(the parity wait would alias)")
+        return self.phase > index
+
+
+def tile_nkv(N, causal, q0, t):
+    r0 = q0 + t * BQ
+    if r0 >= N:
+        return 0
+    nkv = (N + BK - 1) // BK
+    if not causal:
+        return nkv
+    return (min(N, r0 + BQ) - 1) // BK + 1
+
+
+class Deadlock(AssertionError):
+    pass
+
+
+def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, rescale_prob=0.1):
+    """Run one CTA's item list (first query rows) to completion; raise Deadlock or
+    AssertionError on a protocol fault. ``per_buffer_p=False`` models a single
+    P-ready barrier per tile (a protocol that is known to alias)."""
+    rnd = random.Random(seed)
+    B = {}
+
+    def bar(name, count):
+        B[name] = Bar(name, count)
+
+    for t in range(2):
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", BQ), ("pv_done0", 1),
+                        ("pv_done1", 1)):
+            bar(f"{name}{t}", c)
+        if per_buffer_p:
+            bar(f"p_full{t}0", BQ)
+            bar(f"p_full{t}1", BQ)
+        else:
+            bar(f"p_full{t}", BQ)
+    for s in range(ring):
+        bar(f"k_full{s}", 1)
+        bar(f"k_empty{s}", 2)
+        bar(f"v_full{s}", 1)
+        bar(f"v_empty{s}", 2)
+    tensor_pipe, tma = [], []
+
+    def p_full_name(t, g):
+        return (f"p_full{t}{g & 1}", g >> 1) if per_buffer_p else (f"p_full{t}", g)
+
+    def counts(q0):
+        n = [tile_nkv(N, causal, q0, t) for t in range(2)]
+        return n, max(n)
+
+    def producer():
+        qcount, kpos, vpos = [0, 0], 0, 0
+        for q0 in items:
+            n, nmax = counts(q0)
+            for t in range(2):
+                if n[t]:
+                    yield ("wait", f"q_empty{t}", qcount[t] - 1)
+                    tma.append(f"q_full{t}")
+                    qcount[t] += 1
+            order = ["K"] + [x for j in range(nmax) for x in (["K"] if j + 1 < nmax else []) + ["V"]]
+            for kind in order:
+                if kind == "K":
+                    yield ("wait", f"k_empty{kpos % ring}", kpos // ring - 1)
+                    tma.append(f"k_full{kpos % ring}")
+                    kpos += 1
+                else:
+                    yield ("wait", f"v_empty{vpos % ring}", vpos // ring - 1)
+                    tma.append(f"v_full{vpos % ring}")
+                    vpos += 1
+
+    def s_issuer(t):
+        qcount = issued = kpos = 0
+        for q0 in items:
+            n, nmax = counts(q0)
+            if n[t]:
+                yield ("wait", f"q_full{t}", qcount)
+                qcount += 1
+            for j in range(nmax):
+                s = kpos % ring
+                yield ("wait", f"k_full{s}", kpos // ring)
+                kpos += 1
+                if j >= n[t]:
+                    yield ("arrive", f"k_empty{s}", 1)
+                    continue
+                if issued:
+                    yield ("wait", f"s_free{t}", issued - 1)
+                issued += 1
+                tensor_pipe.extend([("commit", f"s_full{t}")] + ([("commit", f"q_empty{t}")] if j == n[t] - 1 else [])
+                                   + [("commit", f"k_empty{s}")])
+
+    def pv_issuer(t):
+        g = vpos = 0
+        for q0 in items:
+            n, nmax = counts(q0)
+            for j in range(nmax):
+                s = vpos % ring
+                yield ("wait", f"v_full{s}", vpos // ring)
+                vpos += 1
+                if j >= n[t]:
+                    yield ("arrive", f"v_empty{s}", 1)
+                    continue
+                yield ("wait",) + p_full_name(t, g)
+                tensor_pipe.extend([("commit", f"pv_done{t}{g & 1}"), ("commit", f"v_empty{s}")])
+                g += 1
+
+    def softmax(t):
+        scount = g = 0
+        for q0 in items:
+            n, _ = counts(q0)
+            if not n[t]:
+                continue
+            for j in range(n[t]):
+                yield ("wait", f"s_full{t}", scount)
+                scount += 1
+                yield ("arrive", f"s_free{t}", BQ // softmax_warps)
+                if j > 0 and rnd.random() < rescale_prob:  # O rescale needs the previous product
+                    yield ("wait", f"pv_done{t}{(g - 1) & 1}", (g - 1) >> 1)
+                if g >= 2:  # P buffer g & 1 was last read by product g - 2
+                    yield ("wait", f"pv_done{t}{g & 1}", (g - 2) >> 1)
+                yield ("arrive", p_full_name(t, g)[0], BQ // softmax_warps)
+                g += 1
+            yield ("wait", f"pv_done{t}{(g - 1) & 1}", (g - 1) >> 1)  # epilogue
+
+    agents = {"producer": producer(), "S0": s_issuer(0), "S1": s_issuer(1), "PV0": pv_issuer(0),
+              "PV1": pv_issuer(1)}
+    for t in range(2):
+        for w in range(softmax_warps):
+            agents[f"softmax{t}.{w}"] = softmax(t)
+    waiting = {k: None for k in agents}
+    while agents or tensor_pipe or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        if tensor_pipe:
+            ready.append("#tensor")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c == "#tensor":
+            _, name = tensor_pipe.pop(0)
+            B[name].arrive(1)
+            continue
+        if c == "#tma":
+            B[tma.pop(rnd.randrange(len(tma)))].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

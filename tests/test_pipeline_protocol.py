@@ -1,0 +1,37 @@
+"""The forward kernel's barrier protocol, checked on a CPU model (no GPU).
+
+tests/pipeline_model.py restates the order of every wait and arrival of the
+kernel's roles; here random interleavings of it must finish without a deadlock
+and without any parity wait that could alias. A variant with a single P-ready
+barrier per tile (an earlier protocol that let the softmax run two blocks
+ahead of the PV issuer) must be caught, which shows the check has teeth.
+"""
+import pytest
+
+from pipeline_model import ROWS, simulate
+
+
+def _items(N, all_blocks):
+    nqb = (N + ROWS - 1) // ROWS
+    if not all_blocks:
+        return [(nqb - 1) * ROWS]
+    return [qb * ROWS for qb in range(nqb - 1, -1, -1)]  # longest first, as the kernel schedules
+
+
+@pytest.mark.parametrize("N,causal", [(1000, True), (8192, True), (384, True), (200, True), (129, False),
+                                      (1000, False), (64, False), (1, True)])
+@pytest.mark.parametrize("ring", [2, 5, 6])
+def test_protocol_completes_without_aliasing(N, causal, ring):
+    for all_blocks in (False, True):
+        for seed in range(6 if N <= 1000 else 2):
+            assert simulate(N, causal, _items(N, all_blocks), ring, seed)
+
+
+def test_single_p_barrier_is_caught():
+    caught = 0
+    for seed in range(10):
+        try:
+            simulate(1000, True, _items(1000, False), 5, seed, per_buffer_p=False)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
