@@ -39,7 +39,8 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from io_aware_exact_13_gb300.inputs import HEADLINE, WORKLOADS, make_workload, sample_rows  # noqa: E402
+from io_aware_exact_13_gb300.inputs import (DECODE_WORKLOADS, HEADLINE, WORKLOADS, make_decode,  # noqa: E402
+                                            make_workload, sample_rows)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
 UNIT = "TFLOP/s"
@@ -55,6 +56,14 @@ def kernel_source_hash() -> str:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def load_hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured copy bandwidth (MEASURED_PEAKS.json)"
+    except Exception:
+        return 6800.0, "fallback 6.8 TB/s (no measured peak file)"
 
 
 def load_peak():
@@ -334,17 +343,67 @@ def run_ours(args, w):
     return 0
 
 
+def run_decode(args, w):
+    """Split-KV decoding forward: HBM-bound (every K and V byte read once per call)."""
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from io_aware_exact_13_gb300 import fa
+
+    q, k, v = make_decode(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    n_splits = fa.fa_splitkv_num_splits(w.B, w.H, w.Nq, w.Nk, w.d)
+    ws = torch.empty(fa.fa_splitkv_workspace_bytes(w.B, w.H, w.Nq, w.d, n_splits), dtype=torch.uint8, device=dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    entry = fa.fa_fwd_splitkv if w.dtype == "bf16" else fa.fa_fwd_splitkv_fp16
+
+    def step():
+        entry(qd, kd, vd, od, lsed, w.scale, w.causal, n_splits, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(world, a.elapsed_time(b), dev) / args.steps
+    if rank != 0:
+        return 0
+    peak, src = load_hbm_peak()
+    bytes_alg = w.kv_bytes + 2 * qd.numel() * qd.element_size() + lsed.numel() * 4
+    gbs = bytes_alg / (ms * 1e-3) / 1e9
+    line = {"metric": "split-KV decode effective HBM GB/s", "value": world * gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(w.describe(), n_splits=n_splits,
+                           l2="K/V (%.0f MB) exceed the 126 MB L2; no flush" % (w.kv_bytes / 1e6)),
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "peak_source": src, "kernel": "fa_splitkv_partial + fa_splitkv_combine",
+                         "tflops": w.flops / (ms * 1e-3) / 1e12}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.workload in DECODE_WORKLOADS:
+        return run_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

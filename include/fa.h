@@ -51,7 +51,8 @@ typedef enum {
     FA_ERR_SHAPE = -3,       /* B, H or N < 1, or a size overflows its limit */
     FA_ERR_UNSUPPORTED = -4, /* d not supported for this element type */
     FA_ERR_LAUNCH = -5,      /* the CUDA launch (or tensor-map encoding) failed */
-    FA_ERR_TIMEOUT = -6      /* a device-side wait gave up (device status word) */
+    FA_ERR_TIMEOUT = -6,     /* a device-side wait gave up (device status word) */
+    FA_ERR_WORKSPACE = -7    /* workspace missing or smaller than the problem needs */
 } fa_status;
 
 /* bf16 Q/K/V/out, fp32 accumulation. d in {64, 128}. */
@@ -66,6 +67,37 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_o
  * rounding of the inputs). d in {64, 128}; B*H must not exceed 65535. */
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                 float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* ---- split-KV forward for decoding ------------------------------------------
+ * Same operation for Nq query rows (1 <= Nq <= 16) against Nk >= 1 keys:
+ *   q, out : [B][H][Nq][d]      k, v : [B][H][Nk][d]      lse : float [B][H][Nq]
+ * causal != 0 aligns the last query with the last key: query i sees keys
+ * j <= i + (Nk - Nq); otherwise every query sees every key. No mask argument.
+ * The key range is cut into n_splits contiguous blocks; each block's summary
+ * (its partial output and log-sum-exp) is written to `workspace`, and a second
+ * kernel merges the summaries onto their common maximum ("FlashAttention"
+ * glossary, sections "Why a tile can be discarded" and "Practice: can you
+ * average block outputs?"). The result equals the unsplit attention.
+ * workspace: caller-owned device memory, 256-byte aligned, of at least
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, n_splits) bytes; its contents on
+ * entry do not matter and are overwritten. Calls that share a workspace must
+ * not overlap on the GPU. B*H <= 65535, 1 <= n_splits <= Nk. */
+
+/* A split count that gives the GPU enough independent blocks (>= 1). */
+int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d);
+
+/* Workspace bytes fa_fwd_splitkv needs, or a negative status. */
+long long fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
+
+/* bf16 q/k/v/out, fp32 accumulation. d in {64, 128}. */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Nq,
+                   int Nk, int d, float scale, int causal, int n_splits, void *workspace,
+                   unsigned long long workspace_bytes, void *stream);
+
+/* fp16 q/k/v/out, fp32 accumulation. d in {64, 128}. */
+int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                        int Nq, int Nk, int d, float scale, int causal, int n_splits, void *workspace,
+                        unsigned long long workspace_bytes, void *stream);
 
 /* Static text for a status code (never NULL). */
 const char *fa_status_string(int status);

@@ -10,6 +10,7 @@
 
 #include "../../include/fa.h"
 #include "fa_launch.cuh"
+#include "fa_splitkv.cuh"
 
 namespace fa {
 int launch_fwd_bf16(const LaunchArgs &a);
@@ -116,6 +117,47 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
     return rc;
 }
 
+int check_splitkv(const void *q, const void *k, const void *v, const void *out, const float *lse, int B, int H,
+                  int Nq, int Nk, int d, int n_splits) {
+    if (!q || !k || !v || !out || !lse) return FA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+        return FA_ERR_ALIGN;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || Nq > fa::kSplitKVMaxNq) return FA_ERR_SHAPE;
+    if (static_cast<int64_t>(B) * H > 65535) return FA_ERR_SHAPE;
+    if (n_splits < 1 || n_splits > Nk || n_splits > 65535) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+int splitkv_common(bool fp16, const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                   int Nq, int Nk, int d, float scale, int causal, int n_splits, void *workspace,
+                   unsigned long long workspace_bytes, void *stream) {
+    int rc = check_splitkv(q, k, v, out, lse, B, H, Nq, Nk, d, n_splits);
+    if (rc != FA_OK) return rc;
+    const int64_t rows = static_cast<int64_t>(B) * H * Nq;
+    const size_t need = fa::splitkv_workspace_bytes(rows, d, n_splits);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    fa::SplitKVArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.n_splits = n_splits;
+    const size_t o_bytes = ((static_cast<size_t>(n_splits) * rows * d * sizeof(float) + 255) / 256) * 256;
+    a.o_part = static_cast<float *>(workspace);
+    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
+    a.stream = static_cast<cudaStream_t>(stream);
+    return fa::launch_splitkv(a, fp16);
+}
+
 }  // namespace
 
 namespace fa {
@@ -152,6 +194,41 @@ int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_o
     return fwd_common(Type::FP32, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
 }
 
+int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d) {
+    (void)Nq;
+    (void)d;
+    if (B < 1 || H < 1 || Nk < 1) return FA_ERR_SHAPE;
+    DeviceInfo *di = device_info();
+    const int64_t sms = di ? di->num_sms : 148;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    int64_t n = (4 * sms + bh - 1) / bh;  // about four CTAs per SM
+    const int64_t max_by_len = (static_cast<int64_t>(Nk) + 63) / 64;  // at least ~64 keys per split
+    if (n > max_by_len) n = max_by_len;
+    if (n > 1024) n = 1024;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
+long long fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int n_splits) {
+    if (B < 1 || H < 1 || Nq < 1 || n_splits < 1) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return static_cast<long long>(
+        fa::splitkv_workspace_bytes(static_cast<int64_t>(B) * H * Nq, d, n_splits));
+}
+
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Nq,
+                   int Nk, int d, float scale, int causal, int n_splits, void *workspace,
+                   unsigned long long workspace_bytes, void *stream) {
+    return splitkv_common(false, q, k, v, out, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace,
+                          workspace_bytes, stream);
+}
+
+int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                        int Nq, int Nk, int d, float scale, int causal, int n_splits, void *workspace,
+                        unsigned long long workspace_bytes, void *stream) {
+    return splitkv_common(true, q, k, v, out, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace,
+                          workspace_bytes, stream);
+}
+
 const char *fa_status_string(int status) {
     switch (status) {
         case FA_OK: return "ok";
@@ -161,6 +238,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_UNSUPPORTED: return "unsupported head dimension for this element type";
         case FA_ERR_LAUNCH: return "CUDA launch or tensor-map encoding failed";
         case FA_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
+        case FA_ERR_WORKSPACE: return "workspace missing or smaller than the problem needs";
         default: return "unknown status";
     }
 }

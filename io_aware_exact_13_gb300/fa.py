@@ -6,9 +6,10 @@ There is no CPU fallback: importing this module fails loudly when the library
 has not been built, and every call raises if the library returns an error.
 
 Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
+``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), their sizing helpers,
 ``fa_status_string``, ``fa_get_device_status``, ``fa_num_sms``. ``attention``
-is a convenience wrapper that allocates O and lse with torch and picks the
-entry point from the input dtype.
+and ``attention_decode`` are convenience wrappers that allocate outputs (and
+the split-KV workspace) with torch and pick the entry point from the dtype.
 """
 from __future__ import annotations
 
@@ -32,6 +33,7 @@ FA_ERR_SHAPE = -3
 FA_ERR_UNSUPPORTED = -4
 FA_ERR_LAUNCH = -5
 FA_ERR_TIMEOUT = -6
+FA_ERR_WORKSPACE = -7
 
 # Every symbol the header declares, with its ctypes signature.
 _vp = ctypes.c_void_p
@@ -44,6 +46,12 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_get_device_status": (ctypes.c_int, [_vp]),
     "fa_num_sms": (ctypes.c_int, []),
+    "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int] * 5),
+    "fa_splitkv_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 5),
+    "fa_fwd_splitkv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
+                       [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_fwd_splitkv_fp16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
+                            [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
 }
 for _name, (_res, _args) in SIGNATURES.items():
     _f = getattr(lib, _name)
@@ -123,6 +131,72 @@ def attention(q, k, v, mask=None, scale=None, causal=False, out=None, lse=None, 
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
+    return out, lse
+
+
+# ---------------------------------------------------------------- split-KV decoding
+def fa_splitkv_num_splits(B, H, Nq, Nk, d) -> int:
+    n = int(lib.fa_splitkv_num_splits(int(B), int(H), int(Nq), int(Nk), int(d)))
+    if n < 0:
+        raise FAError(n, "fa_splitkv_num_splits")
+    return n
+
+
+def fa_splitkv_workspace_bytes(B, H, Nq, d, n_splits) -> int:
+    n = int(lib.fa_splitkv_workspace_bytes(int(B), int(H), int(Nq), int(d), int(n_splits)))
+    if n < 0:
+        raise FAError(n, "fa_splitkv_workspace_bytes")
+    return n
+
+
+def _check_splitkv(q, k, v, out, lse, dtype):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("q, out must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k, v must be [B, H, Nk, d] with q's B, H, d")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, Nq):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, Nq] tensor")
+    return B, H, Nq, k.shape[2], d
+
+
+def _raw_splitkv(fn_name, q, k, v, out, lse, scale, causal, n_splits, workspace, stream, dtype):
+    B, H, Nq, Nk, d = _check_splitkv(q, k, v, out, lse, dtype)
+    if workspace is None or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, float(scale),
+                               int(bool(causal)), int(n_splits), _ptr(workspace), nbytes,
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_splitkv(q, k, v, out, lse, scale, causal, n_splits, workspace, stream=None):
+    """bf16 split-KV forward (Nq <= 16 query rows, Nk keys) into ``out`` and ``lse``."""
+    _raw_splitkv("fa_fwd_splitkv", q, k, v, out, lse, scale, causal, n_splits, workspace, stream, torch.bfloat16)
+
+
+def fa_fwd_splitkv_fp16(q, k, v, out, lse, scale, causal, n_splits, workspace, stream=None):
+    """fp16 split-KV forward into ``out`` and ``lse``."""
+    _raw_splitkv("fa_fwd_splitkv_fp16", q, k, v, out, lse, scale, causal, n_splits, workspace, stream,
+                 torch.float16)
+
+
+def attention_decode(q, k, v, scale=None, causal=False, n_splits=None, stream=None):
+    """Split-KV forward for few query rows; the workspace is a torch allocation."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    n_splits = fa_splitkv_num_splits(B, H, Nq, Nk, d) if n_splits is None else n_splits
+    ws = torch.empty(fa_splitkv_workspace_bytes(B, H, Nq, d, n_splits), dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fn = {torch.bfloat16: fa_fwd_splitkv, torch.float16: fa_fwd_splitkv_fp16}[q.dtype]
+    fn(q, k, v, out, lse, scale, causal, n_splits, ws, stream)
     return out, lse
 
 

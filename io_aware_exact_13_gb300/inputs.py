@@ -73,6 +73,50 @@ WORKLOADS = {
 HEADLINE = "b1h32_n8192_d128_bf16_causal"
 
 
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Few query rows (Nq) against a long key/value sequence (Nk)."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def kv_bytes(self) -> int:
+        """K and V bytes, each read once per call."""
+        return 2 * self.B * self.H * self.Nk * self.d * (4 if self.dtype == "fp32" else 2)
+
+    @property
+    def flops(self) -> float:
+        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "Nq": self.Nq, "Nk": self.Nk, "d": self.d,
+                "dtype": self.dtype, "causal": self.causal}
+
+
+DECODE_WORKLOADS = {
+    "decode_b8h32_nq1_nk32768_d128_bf16": DecodeWorkload("decode_b8h32_nq1_nk32768_d128_bf16", 8, 32, 1, 32768,
+                                                         128, "bf16", False, 2001),
+    "decode_b4h32_nq4_nk8192_d128_bf16_causal": DecodeWorkload("decode_b4h32_nq4_nk8192_d128_bf16_causal", 4, 32,
+                                                               4, 8192, 128, "bf16", True, 2002),
+}
+
+
+def make_decode(w: DecodeWorkload):
+    q, k, v, _ = make_qkv(w.B, w.H, w.Nq, w.d, w.dtype, w.seed, Nk=w.Nk)
+    return q, k, v
+
+
 def make_qkv(B, H, N, d, dtype="bf16", seed=0, mul=1.0, k_offset=0.0, mask_frac=0.0, full_row_frac=0.0,
              Nk: Optional[int] = None):
     """Draw (q, k, v, mask_or_None) on the CPU following the recipe above.

@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_forward_family():
     names = declared_functions()
-    for n in ("fa_fwd", "fa_fwd_fp16", "fa_fwd_fp32", "fa_status_string", "fa_get_device_status", "fa_num_sms"):
+    for n in ("fa_fwd", "fa_fwd_fp16", "fa_fwd_fp32", "fa_status_string", "fa_get_device_status", "fa_num_sms",
+              "fa_fwd_splitkv", "fa_fwd_splitkv_fp16", "fa_splitkv_workspace_bytes", "fa_splitkv_num_splits"):
         assert n in names
 
 
@@ -40,7 +41,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 
 def test_status_strings(fa):
-    for code in range(0, -7, -1):
+    for code in range(0, -8, -1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(12345) == "unknown status"
@@ -73,6 +74,33 @@ def test_host_validation_rejects_before_launch(fa, name):
 
 def test_fp32_grid_limit(fa):
     assert _call(fa, "fa_fwd_fp32", B=256, H=257) == fa.FA_ERR_SHAPE
+
+
+def test_splitkv_host_checks(fa):
+    lib = fa.lib
+    assert lib.fa_splitkv_workspace_bytes(1, 1, 1, 96, 4) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_splitkv_workspace_bytes(0, 1, 1, 64, 4) == fa.FA_ERR_SHAPE
+    rows, d, n = 2 * 3 * 5, 128, 7
+    expect = ((n * rows * d * 4 + 255) // 256) * 256 + ((n * rows * 4 + 255) // 256) * 256
+    assert lib.fa_splitkv_workspace_bytes(2, 3, 5, d, n) == expect
+
+    def call(name="fa_fwd_splitkv", q=0x10000, Nq=1, Nk=64, d=128, n_splits=2, ws=0x100000, ws_bytes=1 << 20):
+        f = getattr(lib, name)
+        return f(ctypes.c_void_p(q) if q else None, ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000),
+                 ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000), 1, 2, Nq, Nk, d, ctypes.c_float(0.1), 0,
+                 n_splits, ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+    for name in ("fa_fwd_splitkv", "fa_fwd_splitkv_fp16"):
+        assert call(name, q=0) == fa.FA_ERR_NULL
+        assert call(name, q=0x10008) == fa.FA_ERR_ALIGN
+        assert call(name, Nq=17) == fa.FA_ERR_SHAPE
+        assert call(name, Nq=0) == fa.FA_ERR_SHAPE
+        assert call(name, n_splits=0) == fa.FA_ERR_SHAPE
+        assert call(name, n_splits=65) == fa.FA_ERR_SHAPE  # more splits than keys
+        assert call(name, d=80) == fa.FA_ERR_UNSUPPORTED
+        assert call(name, ws=0) == fa.FA_ERR_WORKSPACE
+        assert call(name, ws=0x100010) == fa.FA_ERR_WORKSPACE  # not 256-byte aligned
+        assert call(name, ws_bytes=16) == fa.FA_ERR_WORKSPACE
 
 
 def test_binding_checks_shapes_without_a_gpu(fa):
