@@ -99,6 +99,23 @@ int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, 
                         int Nq, int Nk, int d, float scale, int causal, int n_splits, void *workspace,
                         unsigned long long workspace_bytes, void *stream);
 
+/* bf16 split-KV forward that allocates nothing and takes no workspace (the
+ * method's pages have no counterpart of this entry point; it exists for
+ * callers that cannot allocate device memory where they call attention: a
+ * host framework that owns every device allocation through its own pool, a
+ * serving loop in which cudaMalloc's implicit device-wide synchronisation
+ * would stall other work, or an embedded host with a fixed memory budget).
+ * Same arguments and results as fa_fwd_splitkv minus the workspace: the
+ * per-split scratch lives in one 16 MiB device array inside the library, which
+ * every GPU that loads the library holds until exit. Problems whose scratch,
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, n_splits), exceeds 16 MiB are
+ * rejected with FA_ERR_WORKSPACE. The first call on a device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture. All calls share the array: calls that overlap
+ * on the GPU race and must be serialised by the caller. */
+int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                           int Nq, int Nk, int d, float scale, int causal, int n_splits, void *stream);
+
 /* Static text for a status code (never NULL). */
 const char *fa_status_string(int status);
 

@@ -52,6 +52,8 @@ SIGNATURES = {
                        [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
     "fa_fwd_splitkv_fp16": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
                             [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
+    "fa_fwd_splitkv_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
+                               [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
 }
 for _name, (_res, _args) in SIGNATURES.items():
     _f = getattr(lib, _name)
@@ -184,6 +186,19 @@ def fa_fwd_splitkv_fp16(q, k, v, out, lse, scale, causal, n_splits, workspace, s
     """fp16 split-KV forward into ``out`` and ``lse``."""
     _raw_splitkv("fa_fwd_splitkv_fp16", q, k, v, out, lse, scale, causal, n_splits, workspace, stream,
                  torch.float16)
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, out, lse, scale, causal, n_splits, stream=None):
+    """bf16 split-KV forward with no workspace: for callers that cannot allocate
+    device memory at the call site (a framework owning all device memory, a
+    serving loop that must not pay cudaMalloc's device-wide synchronisation, a
+    fixed-budget embedded host). The library's fixed 16 MiB scratch array is
+    used instead; calls that overlap on the GPU race on it."""
+    B, H, Nq, Nk, d = _check_splitkv(q, k, v, out, lse, torch.bfloat16)
+    rc = lib.fa_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, float(scale),
+                                    int(bool(causal)), int(n_splits), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_splitkv_noalloc")
 
 
 def attention_decode(q, k, v, scale=None, causal=False, n_splits=None, stream=None):
