@@ -173,15 +173,15 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
                                              const FwdParams &p) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > p.timeout_ns) {
-                *abort_flag = 1;
-                atomicExch(p.status, kStatusTimeout);
-                return false;
-            }
+    for (;;) {
+        // sleep until the phase completes (or 100 us pass) rather than polling, so that
+        // waiting warps leave the issue slots to the warps that are computing
+        if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicExch(p.status, kStatusTimeout);
+            return false;
         }
     }
 }
@@ -528,16 +528,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_ref = m_new;
                 }
                 const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-                float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // exponent arguments and partial sums in packed pairs (one instruction per two keys)
+                const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
+                float2 ls[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
                 uint32_t pv[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float e0 = ex2_approx(fmaf(x[2 * c], sl2, neg));
-                    const float e1 = ex2_approx(fmaf(x[2 * c + 1], sl2, neg));
-                    ls[c & 3] += e0 + e1;
-                    pv[c] = pack2<T>(e0, e1);
+                    const float2 a = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sl2v, negv);
+                    const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                    ls[c & 1] = fadd2(ls[c & 1], e);
+                    pv[c] = pack2<T>(e.x, e.y);
                 }
-                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
                 // P buffer (g & 1) was last read by the product of block g - 2
                 if (g >= 2) {
                     ok = wait_warp(sy.pv_done(t, g & 1u), ((g - 2) >> 1) & 1u, abort_flag, p);
