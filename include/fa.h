@@ -68,6 +68,17 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_o
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                 float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
 
+/* ---- grouped-query attention ------------------------------------------------
+ * Same operation and layouts as fa_fwd / fa_fwd_fp16, except that k and v hold
+ * Hkv heads, [B][Hkv][N][d], each shared by H / Hkv consecutive query heads:
+ * query head h reads key/value head h / (H / Hkv). Hkv must divide H; Hkv = H
+ * is plain multi-head attention. (The variant is named by "IO-aware exact
+ * attention", section "Why implementations form a family".) */
+int fa_fwd_gqa(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
+int fa_fwd_gqa_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
+                    float *lse, int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
+
 /* ---- split-KV forward for decoding ------------------------------------------
  * Same operation for Nq query rows (1 <= Nq <= 16) against Nk >= 1 keys:
  *   q, out : [B][H][Nq][d]      k, v : [B][H][Nk][d]      lse : float [B][H][Nq]

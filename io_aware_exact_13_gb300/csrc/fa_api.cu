@@ -87,9 +87,11 @@ int check_args(Type ty, const void *q, const void *k, const void *v, const float
 }
 
 int fwd_common(Type ty, const void *q, const void *k, const void *v, const float *mask, void *out, float *lse,
-               int B, int H, int N, int d, float scale, int causal, void *stream) {
+               int B, int H, int N, int d, float scale, int causal, void *stream, int Hkv = -1) {
     int rc = check_args(ty, q, k, v, mask, out, lse, B, H, N, d);
     if (rc != FA_OK) return rc;
+    if (Hkv == -1) Hkv = H;
+    if (Hkv < 1 || H % Hkv != 0) return FA_ERR_SHAPE;
     DeviceInfo *di = device_info();
     if (!di || !encoder()) return FA_ERR_LAUNCH;
     fa::LaunchArgs a;
@@ -103,6 +105,7 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
     a.H = H;
     a.N = N;
     a.d = d;
+    a.Hkv = Hkv;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.stream = static_cast<cudaStream_t>(stream);
@@ -227,6 +230,18 @@ int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, 
                         unsigned long long workspace_bytes, void *stream) {
     return splitkv_common(true, q, k, v, out, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace,
                           workspace_bytes, stream);
+}
+
+int fa_fwd_gqa(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
+               int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream) {
+    if (Hkv < 1) return FA_ERR_SHAPE;
+    return fwd_common(Type::BF16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream, Hkv);
+}
+
+int fa_fwd_gqa_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
+                    int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream) {
+    if (Hkv < 1) return FA_ERR_SHAPE;
+    return fwd_common(Type::FP16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream, Hkv);
 }
 
 const char *fa_status_string(int status) {

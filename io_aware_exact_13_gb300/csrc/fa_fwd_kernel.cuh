@@ -110,6 +110,7 @@ struct FwdParams {
     const float *mask;  // [B][N][N] or nullptr
     int *status;        // device status word
     int B, H, N;
+    int kv_group;       // query heads per key/value head (1 unless grouped-query attention)
     int n_items;        // B * H * ceil(N / 256)
     int n_qblk;         // ceil(N / 256)
     int n_kv;           // ceil(N / 64)
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_q = policy_evict_first();
             uint32_t qcount[2] = {0, 0};
             uint32_t kpos = 0, vpos = 0;
-            int cur_bh = 0;
+            int cur_bh = 0, kv_bh = 0;
             bool ok = true;
             auto load_kv = [&](bool is_v, int blk) -> bool {
                 uint32_t &pos = is_v ? vpos : kpos;
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
                         tma_load_3d(dst + c * C::KV_CHUNK, is_v ? &tm_v : &tm_k, full, c * C::CHUNK_ELEMS, blk * kBK,
-                                    cur_bh, pol_kv);
+                                    kv_bh, pol_kv);
                 }
                 __syncwarp();
                 ++pos;
@@ -290,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
                 int q0;
                 item_coords(p, item, cur_bh, q0);
+                // grouped-query attention: kv_group consecutive query heads share one K/V head
+                kv_bh = (cur_bh / p.H) * (p.H / p.kv_group) + (cur_bh % p.H) / p.kv_group;
                 const int n0 = tile_nkv<CAUSAL>(p, q0, 0), n1 = tile_nkv<CAUSAL>(p, q0, 1);
                 const int nmax = max(n0, n1);
                 for (int t = 0; t < 2 && ok; ++t) {

@@ -15,6 +15,7 @@ struct LaunchArgs {
     void *out;
     float *lse;
     int B, H, N, d;
+    int Hkv;          // key/value heads (H for plain multi-head attention)
     float scale;
     int causal;
     cudaStream_t stream;
@@ -42,14 +43,16 @@ int launch_variant(const LaunchArgs &a) {
     CUtensorMap tq, tk, tv;
     const int BH = a.B * a.H;
     if (!encode_rows_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.N, BH, kBQ)) return -5;
-    if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BH, kBK)) return -5;
-    if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BH, kBK)) return -5;
+    const int BHkv = a.B * a.Hkv;
+    if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BHkv, kBK)) return -5;
+    if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BHkv, kBK)) return -5;
     FwdParams p;
     p.out = a.out;
     p.lse = a.lse;
     p.mask = a.mask;
     p.status = a.status;
     p.B = a.B;
+    p.kv_group = a.H / a.Hkv;
     p.H = a.H;
     p.N = a.N;
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;

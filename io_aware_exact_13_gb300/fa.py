@@ -46,6 +46,8 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_get_device_status": (ctypes.c_int, [_vp]),
     "fa_num_sms": (ctypes.c_int, []),
+    "fa_fwd_gqa": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
+    "fa_fwd_gqa_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int] * 5),
     "fa_splitkv_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 5),
     "fa_fwd_splitkv": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
@@ -134,6 +136,36 @@ def attention(q, k, v, mask=None, scale=None, causal=False, out=None, lse=None, 
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
     return out, lse
+
+
+# ---------------------------------------------------------------- grouped-query attention
+def _fwd_gqa(fn_name, dtype, q, k, v, mask_or_null, out, lse, scale, causal, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape or out.shape != q.shape or H % Hkv:
+        raise ValueError("q, out: [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, N] tensor")
+    if mask_or_null is not None and (mask_or_null.dtype != torch.float32 or mask_or_null.shape != (B, N, N)
+                                     or not mask_or_null.is_contiguous() or not mask_or_null.is_cuda):
+        raise ValueError("mask must be a contiguous CUDA float32 [B, N, N] tensor")
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(mask_or_null), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                               float(scale), int(bool(causal)), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_gqa(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
+    """bf16 grouped-query forward: k, v are [B, Hkv, N, d], shared by H / Hkv query heads each."""
+    _fwd_gqa("fa_fwd_gqa", torch.bfloat16, q, k, v, mask_or_null, out, lse, scale, causal, stream)
+
+
+def fa_fwd_gqa_fp16(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
+    """fp16 grouped-query forward."""
+    _fwd_gqa("fa_fwd_gqa_fp16", torch.float16, q, k, v, mask_or_null, out, lse, scale, causal, stream)
 
 
 # ---------------------------------------------------------------- split-KV decoding

@@ -76,6 +76,16 @@ def test_fp32_grid_limit(fa):
     assert _call(fa, "fa_fwd_fp32", B=256, H=257) == fa.FA_ERR_SHAPE
 
 
+def test_gqa_host_checks(fa):
+    f = fa.lib.fa_fwd_gqa
+    args = lambda H, Hkv: (ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000), None,
+                           ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000), 1, H, Hkv, 64, 128,
+                           ctypes.c_float(0.1), 0, None)
+    assert f(*args(8, 3)) == fa.FA_ERR_SHAPE   # Hkv must divide H
+    assert f(*args(8, 0)) == fa.FA_ERR_SHAPE
+    assert fa.lib.fa_fwd_gqa_fp16(*args(4, 8)) == fa.FA_ERR_SHAPE
+
+
 def test_splitkv_host_checks(fa):
     lib = fa.lib
     assert lib.fa_splitkv_workspace_bytes(1, 1, 1, 96, 4) == fa.FA_ERR_UNSUPPORTED
