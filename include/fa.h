@@ -127,6 +127,34 @@ int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, 
 int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
                            int Nq, int Nk, int d, float scale, int causal, int n_splits, void *stream);
 
+/* ---- backward by recomputation ---------------------------------------------
+ * Gradients of L = sum(dout o out) for out = softmax(scale Q K^T) V ("IO-aware
+ * exact attention", section "Backward recomputation"): from q, k, v, the
+ * forward's out and lse, and dout, every score and probability tile is
+ * rebuilt on chip (P = exp(scale Q K^T - lse)), so no N x N tensor is stored:
+ *   dV = P^T dout,  dS = P o (dout V^T - D),  D_i = sum_t dout_it out_it,
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ * Layouts: q, k, v, out, dout, dq, dk, dv : [B][H][N][d], one element type per
+ * entry point (bf16 / fp16); lse : float [B][H][N] as written by fa_fwd.
+ * All are DEVICE pointers, caller-owned, 16-byte aligned (lse 4). No mask
+ * argument; causal as in fa_fwd. Every query row must see at least one key
+ * (true without a mask), so that lse is finite.
+ * workspace: caller-owned device memory, 256-byte aligned, of at least
+ * fa_bwd_workspace_bytes(B, H, N, d) bytes (an fp32 dQ accumulator of
+ * B*H*N*d floats plus two per-row fp32 arrays); contents on entry do not
+ * matter. Calls sharing a workspace must not overlap on the GPU. Four kernels
+ * are enqueued on `stream`: row statistics, the tiled backward, and the
+ * conversion of the dQ accumulator. d in {64, 128}.
+ * Errors as for fa_fwd; FA_ERR_WORKSPACE if the workspace is missing, too
+ * small or misaligned. */
+long long fa_bwd_workspace_bytes(int B, int H, int N, int d);
+int fa_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+           void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
+           unsigned long long workspace_bytes, void *stream);
+int fa_bwd_fp16(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
+                void *workspace, unsigned long long workspace_bytes, void *stream);
+
 /* Static text for a status code (never NULL). */
 const char *fa_status_string(int status);
 

@@ -10,6 +10,7 @@
 
 #include "../../include/fa.h"
 #include "fa_launch.cuh"
+#include "fa_bwd.cuh"
 #include "fa_splitkv.cuh"
 
 namespace fa {
@@ -161,6 +162,52 @@ int splitkv_common(bool fp16, const void *q, const void *k, const void *v, void 
     return fa::launch_splitkv(a, fp16);
 }
 
+int bwd_common(bool fp16, const void *q, const void *k, const void *v, const void *out, const void *dout,
+               const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
+               void *workspace, unsigned long long workspace_bytes, void *stream) {
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(dout, 16) ||
+        !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+        return FA_ERR_ALIGN;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (bh > INT32_MAX) return FA_ERR_SHAPE;
+    const int64_t npad = fa::bwd_padded_rows(N);
+    if (bh * (npad / fa::kBwdRows) > INT32_MAX) return FA_ERR_SHAPE;  // one CTA per (head, 128-key block)
+    if (bh * npad > (int64_t(1) << 36)) return FA_ERR_SHAPE;           // row-statistics grid
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const size_t need = fa::bwd_workspace_bytes(bh, N, d);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    DeviceInfo *di = device_info();
+    if (!di || !encoder()) return FA_ERR_LAUNCH;
+    fa::BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    const size_t acc = static_cast<size_t>(bh) * static_cast<size_t>(N) * static_cast<size_t>(d) * sizeof(float);
+    const size_t row = static_cast<size_t>(bh) * static_cast<size_t>(npad) * sizeof(float);
+    char *ws = static_cast<char *>(workspace);
+    a.dq_acc = reinterpret_cast<float *>(ws);
+    a.lse2 = reinterpret_cast<float *>(ws + ((acc + 255) / 256) * 256);
+    a.dsum = reinterpret_cast<float *>(ws + ((acc + 255) / 256) * 256 + ((row + 255) / 256) * 256);
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status = di->status;
+    a.timeout_ns = kDefaultTimeoutNs;
+    return fa::launch_bwd(a, fp16);
+}
+
 }  // namespace
 
 namespace fa {
@@ -242,6 +289,26 @@ int fa_fwd_gqa_fp16(const void *q, const void *k, const void *v, const float *ma
                     int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream) {
     if (Hkv < 1) return FA_ERR_SHAPE;
     return fwd_common(Type::FP16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream, Hkv);
+}
+
+long long fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    return static_cast<long long>(fa::bwd_workspace_bytes(static_cast<int64_t>(B) * H, N, d));
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+           void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
+           unsigned long long workspace_bytes, void *stream) {
+    return bwd_common(false, q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes, stream);
+}
+
+int fa_bwd_fp16(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
+                unsigned long long workspace_bytes, void *stream) {
+    return bwd_common(true, q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes, stream);
 }
 
 const char *fa_status_string(int status) {

@@ -164,6 +164,12 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, uint32_t M, u
            | ((M >> 4) << 24);       // M / 16
 }
 
+// Same, with the major-ness of A selectable too (A stored M-contiguous when a_mn_major).
+__host__ __device__ constexpr uint32_t make_idesc_ab(uint32_t ab_fmt, uint32_t M, uint32_t N, uint32_t a_mn_major,
+                                                     uint32_t b_mn_major) {
+    return make_idesc(ab_fmt, M, N, b_mn_major) | (a_mn_major << 15);
+}
+
 // TMEM address: lane in bits 31..16, column in bits 15..0.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
@@ -171,6 +177,8 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
 
 #define FA_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
                  "=r"(r[i + 6]), "=r"(r[i + 7])
+#define FA_S8(i) "=r"(s[i + 0]), "=r"(s[i + 1]), "=r"(s[i + 2]), "=r"(s[i + 3]), "=r"(s[i + 4]), "=r"(s[i + 5]), \
+                 "=r"(s[i + 6]), "=r"(s[i + 7])
 #define FA_RW8(i) "+r"(r[i + 0]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]), \
                   "+r"(r[i + 6]), "+r"(r[i + 7])
 #define FA_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
@@ -187,6 +195,22 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
         "tcgen05.wait::ld.sync.aligned;"
         : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24)
         : "r"(taddr)
+        : "memory");
+}
+
+// Two 32-column loads from unrelated column offsets, then one wait.
+__device__ __forceinline__ void tmem_ld32x2_wait(uint32_t taddr_a, uint32_t (&r)[32], uint32_t taddr_b,
+                                                 uint32_t (&s)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), FA_S8(0), FA_S8(8), FA_S8(16), FA_S8(24)
+        : "r"(taddr_a), "r"(taddr_b)
         : "memory");
 }
 
@@ -244,12 +268,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         FA_W8(0), FA_W8(8), FA_W8(16), FA_W8(24)
         : "memory");
 }
+// Each thread writes 16 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        FA_W8(0), FA_W8(8)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 #undef FA_R8
 #undef FA_RW8
+#undef FA_S8
 #undef FA_W8
 
 // ------------------------------------------------------------------ math
@@ -298,6 +331,18 @@ __device__ __forceinline__ float4 ld_global_nc_v4(const float *ptr) {
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(ptr));
     return v;
+}
+
+// Vector atomic add of four fp32 values to global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float *ptr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 template <uint32_t N>

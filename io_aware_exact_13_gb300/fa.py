@@ -6,9 +6,10 @@ There is no CPU fallback: importing this module fails loudly when the library
 has not been built, and every call raises if the library returns an error.
 
 Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
-``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), their sizing helpers,
-``fa_status_string``, ``fa_get_device_status``, ``fa_num_sms``. ``attention``
-and ``attention_decode`` are convenience wrappers that allocate outputs (and
+``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), ``fa_bwd`` /
+``fa_bwd_fp16`` (backward by recomputation), their sizing helpers,
+``fa_status_string``, ``fa_get_device_status``, ``fa_num_sms``. ``attention``,
+``attention_decode`` and ``attention_backward`` are convenience wrappers that allocate outputs (and
 the split-KV workspace) with torch and pick the entry point from the dtype.
 """
 from __future__ import annotations
@@ -56,6 +57,11 @@ SIGNATURES = {
                             [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
     "fa_fwd_splitkv_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
                                [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
+    "fa_bwd_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 4),
+    "fa_bwd": (ctypes.c_int, [_vp] * 9 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp,
+                                                                 ctypes.c_ulonglong, _vp]),
+    "fa_bwd_fp16": (ctypes.c_int, [_vp] * 9 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp,
+                                                                      ctypes.c_ulonglong, _vp]),
 }
 for _name, (_res, _args) in SIGNATURES.items():
     _f = getattr(lib, _name)
@@ -245,6 +251,57 @@ def attention_decode(q, k, v, scale=None, causal=False, n_splits=None, stream=No
     fn = {torch.bfloat16: fa_fwd_splitkv, torch.float16: fa_fwd_splitkv_fp16}[q.dtype]
     fn(q, k, v, out, lse, scale, causal, n_splits, ws, stream)
     return out, lse
+
+
+# ---------------------------------------------------------------- backward (recomputation)
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    n = int(lib.fa_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
+    if n < 0:
+        raise FAError(n, "fa_bwd_workspace_bytes")
+    return n
+
+
+def _raw_bwd(fn_name, dtype, q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError(f"{name} must be [B, H, N, d] like q")
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, N] tensor")
+    if workspace is None or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), B, H, N, d, float(scale), int(bool(causal)), _ptr(workspace), nbytes,
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_bwd(q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream=None):
+    """bf16 backward into caller-provided ``dq``, ``dk``, ``dv`` [B,H,N,d]."""
+    _raw_bwd("fa_bwd", torch.bfloat16, q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream)
+
+
+def fa_bwd_fp16(q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream=None):
+    """fp16 backward into caller-provided ``dq``, ``dk``, ``dv``."""
+    _raw_bwd("fa_bwd_fp16", torch.float16, q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream)
+
+
+def attention_backward(q, k, v, out, dout, lse, scale=None, causal=False, workspace=None, stream=None):
+    """(dq, dk, dv) of sum(dout * out) for out, lse from ``attention``; allocates
+    the outputs and, unless given, the workspace with torch."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fn = {torch.bfloat16: fa_bwd, torch.float16: fa_bwd_fp16}[q.dtype]
+    fn(q, k, v, out, dout, lse, dq, dk, dv, scale, causal, workspace, stream)
+    return dq, dk, dv
 
 
 def fa_get_device_status(stream=None) -> int:

@@ -158,3 +158,53 @@ def sample_rows(total_rows: int, n: int, seed: int = 0) -> torch.Tensor:
     g.manual_seed(int(seed))
     n = min(n, total_rows)
     return torch.randperm(total_rows, generator=g)[:n].sort().values
+
+
+# ---------------------------------------------------------------- backward workloads
+# The backward measurement of "IO-aware exact attention" (section "Backward
+# recomputation", its stored-state vs recomputed exercise): batch 2, 16 heads,
+# head dimension 64, sequence lengths 512 to 4096, identical inputs and loss
+# gradients for every path.
+@dataclass(frozen=True)
+class BwdWorkload:
+    B: int
+    H: int
+    N: int
+    d: int
+    dtype: str = "bf16"
+    causal: bool = False
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops(self) -> float:
+        """Matrix flops of the recomputing backward: five N x N x d products
+        (S, dP, dV, dK, dQ), halved when causal."""
+        f = 5 * 2.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def describe(self) -> dict:
+        return {"B": self.B, "H": self.H, "N": self.N, "d": self.d, "dtype": self.dtype, "causal": self.causal}
+
+
+BWD_WORKLOADS = {
+    f"bwd_b2h16_n{n}_d64_bf16": BwdWorkload(2, 16, n, 64, "bf16", False, seed=400 + n)
+    for n in (512, 1024, 2048, 4096)
+}
+BWD_WORKLOADS["bwd_b2h16_n4096_d64_bf16_causal"] = BwdWorkload(2, 16, 4096, 64, "bf16", True, seed=8300)
+BWD_WORKLOADS["bwd_b1h32_n8192_d128_bf16_causal"] = BwdWorkload(1, 32, 8192, 128, "bf16", True, seed=8301)
+
+
+def make_bwd(B, H, N, d, dtype="bf16", seed=0):
+    """(q, k, v, dout) on the CPU: one CPU generator seeded with ``seed`` draws
+    fp32 standard normals for Q, K, V and then the loss gradient dO, each
+    [B, H, N, d], rounded to the storage dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    t = DTYPES[dtype]
+    out = []
+    for _ in range(4):
+        out.append(torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(t).contiguous())
+    return tuple(out)

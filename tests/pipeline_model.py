@@ -192,3 +192,75 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
             del agents[c]
             waiting[c] = None
     return True
+
+
+def simulate_bwd(n_it, stages, seed, key_warps=4):
+    """The backward kernel's protocol for one CTA (one key block visiting n_it
+    query blocks): TMA producer, MMA issuer, and the key/row warps."""
+    rnd = random.Random(seed)
+    B = {}
+    for name, c in (("kv", 1), ("sp_full", 1), ("p_full", BQ), ("dq_full", 1), ("dq_free", BQ), ("drain", 1)):
+        B[name] = Bar(name, c)
+    for s in range(stages):
+        B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
+        B[f"qd_empty{s}"] = Bar(f"qd_empty{s}", 1)
+    tensor_pipe, tma = [], []
+
+    def producer():
+        tma.append("kv")
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_empty{s}", it // stages - 1)
+            tma.append(f"qd_full{s}")
+
+    def mma():
+        yield ("wait", "kv", 0)
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_full{s}", it // stages)
+            if it > 0:
+                yield ("wait", "dq_free", it - 1)
+            tensor_pipe.append(("commit", "sp_full"))
+            yield ("wait", "p_full", it)
+            tensor_pipe.extend([("commit", "dq_full"), ("commit", f"qd_empty{s}")])
+        tensor_pipe.append(("commit", "drain"))
+        yield ("wait", "drain", 0)
+
+    def keys():
+        for it in range(n_it):
+            yield ("wait", "sp_full", it)
+            yield ("arrive", "p_full", BQ // key_warps)
+            yield ("wait", "dq_full", it)
+            yield ("arrive", "dq_free", BQ // key_warps)
+
+    agents = {"producer": producer(), "mma": mma()}
+    for w in range(key_warps):
+        agents[f"keys{w}"] = keys()
+    waiting = {k: None for k in agents}
+    while agents or tensor_pipe or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        if tensor_pipe:
+            ready.append("#tensor")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c == "#tensor":
+            B[tensor_pipe.pop(0)[1]].arrive(1)
+            continue
+        if c == "#tma":
+            B[tma.pop(rnd.randrange(len(tma)))].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

@@ -130,3 +130,39 @@ def test_product_path_does_not_import_the_oracle():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", txt, re.M), f
                 assert "attn_oracle" not in txt and "liboracle" not in txt, f
+
+
+def _bwd(fa, name="fa_bwd", ptrs=None, B=1, H=1, N=16, d=64, ws=0x90000, ws_bytes=1 << 30):
+    p = [0x10000 * (i + 1) for i in range(9)] if ptrs is None else ptrs
+    f = getattr(fa.lib, name)
+    return f(*[ctypes.c_void_p(x) if x else None for x in p], B, H, N, d, ctypes.c_float(0.125), 0,
+             ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("name", ["fa_bwd", "fa_bwd_fp16"])
+def test_bwd_host_validation_rejects_before_launch(fa, name):
+    base = [0x10000 * (i + 1) for i in range(9)]
+    for i in range(9):
+        p = list(base)
+        p[i] = 0
+        assert _bwd(fa, name, p) == fa.FA_ERR_NULL
+    p = list(base)
+    p[1] += 8
+    assert _bwd(fa, name, p) == fa.FA_ERR_ALIGN
+    p = list(base)
+    p[5] += 2  # lse needs 4 bytes
+    assert _bwd(fa, name, p) == fa.FA_ERR_ALIGN
+    assert _bwd(fa, name, N=0) == fa.FA_ERR_SHAPE
+    assert _bwd(fa, name, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _bwd(fa, name, ws=0) == fa.FA_ERR_WORKSPACE
+    assert _bwd(fa, name, ws=0x90010) == fa.FA_ERR_WORKSPACE  # not 256-byte aligned
+    need = fa.fa_bwd_workspace_bytes(1, 1, 16, 64)
+    assert _bwd(fa, name, ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+
+
+def test_bwd_workspace_size(fa):
+    # fp32 dQ accumulator (B*H*N*d) + two fp32 row arrays padded to 128 rows, each part 256-byte aligned
+    assert fa.fa_bwd_workspace_bytes(2, 16, 4096, 64) == 2 * 16 * 4096 * 64 * 4 + 2 * (2 * 16 * 4096 * 4)
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 64) == 256 + 2 * 512
+    with pytest.raises(fa.FAError):
+        fa.fa_bwd_workspace_bytes(1, 1, 16, 80)

@@ -35,3 +35,12 @@ def test_single_p_barrier_is_caught():
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 7, 32])
+@pytest.mark.parametrize("stages", [2, 3])
+def test_backward_protocol_completes_without_aliasing(n_it, stages):
+    from pipeline_model import simulate_bwd
+
+    for seed in range(20):
+        assert simulate_bwd(n_it, stages, seed)
