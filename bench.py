@@ -39,8 +39,8 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from io_aware_exact_13_gb300.inputs import (DECODE_WORKLOADS, HEADLINE, WORKLOADS, make_decode,  # noqa: E402
-                                            make_workload, sample_rows)
+from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, HEADLINE, WORKLOADS,  # noqa: E402
+                                            make_bwd, make_decode, make_workload, sample_rows)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
 UNIT = "TFLOP/s"
@@ -391,19 +391,143 @@ def run_decode(args, w):
     return 0
 
 
+def materialised_backward(q, k, v, dout, scale, causal):
+    """The stored-state comparison path of the backward measurement, in plain
+    torch ops: S and P are materialised ([B,H,N,N]) by the forward and P is
+    kept for the backward, as a conventional autograd graph does. Returns a
+    callable that runs one backward from the saved P."""
+    N = q.shape[2]
+    s = torch.matmul(q, k.transpose(-1, -2)).float() * scale
+    if causal:
+        s.masked_fill_(torch.ones(N, N, dtype=torch.bool, device=q.device).triu_(1), float("-inf"))
+    p = torch.softmax(s, dim=-1).to(q.dtype)
+    del s
+
+    def backward():
+        dv = torch.matmul(p.transpose(-1, -2), dout)
+        dp = torch.matmul(dout, v.transpose(-1, -2)).float()
+        ds = (p.float() * (dp - (dp * p.float()).sum(-1, keepdim=True))).to(q.dtype)
+        del dp
+        dq = torch.matmul(ds, k) * scale
+        dk = torch.matmul(ds.transpose(-1, -2), q) * scale
+        return dq, dk, dv
+
+    return p, backward
+
+
+def run_bwd(args, w):
+    """Backward by recomputation (three launches per call: row statistics, the
+    tiled tcgen05 backward, dQ conversion) against the materialised path."""
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from io_aware_exact_13_gb300 import fa
+
+    q, k, v, do = make_bwd(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed)
+    qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), do.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    od, lsed = fa.attention(qd, kd, vd, scale=w.scale, causal=w.causal)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    entry = fa.fa_bwd if w.dtype == "bf16" else fa.fa_bwd_fp16
+
+    def step():
+        entry(qd, kd, vd, od, dod, lsed, dq, dk, dv, w.scale, w.causal, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status(stream) != 0:
+        raise SystemExit("device status word set during warm-up")
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(world, a.elapsed_time(b), dev) / args.steps
+    if fa.fa_get_device_status(stream) != 0:
+        raise SystemExit("device status word set in the timed region")
+
+    # peak device memory of one forward + backward, each path on its own
+    def peak_of(fn):
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        fn()
+        torch.cuda.synchronize(dev)
+        return torch.cuda.max_memory_allocated(dev) - base
+
+    def ours_fwd_bwd():
+        o, l = fa.attention(qd, kd, vd, scale=w.scale, causal=w.causal)
+        fa.attention_backward(qd, kd, vd, o, dod, l, scale=w.scale, causal=w.causal)
+
+    def mat_fwd_bwd():
+        p, bwd = materialised_backward(qd, kd, vd, dod, w.scale, w.causal)
+        torch.matmul(p, vd)
+        bwd()
+
+    peak_ours = peak_of(ours_fwd_bwd)
+    peak_mat = peak_of(mat_fwd_bwd)
+    p, bwd = materialised_backward(qd, kd, vd, dod, w.scale, w.causal)
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize(dev)
+    m_steps = max(1, min(args.steps, 50))
+    a.record(stream)
+    for _ in range(m_steps):
+        bwd()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    mat_ms = a.elapsed_time(b) / m_steps
+    del p, bwd
+    if rank != 0:
+        return 0
+    peak, src = load_peak()
+    tflops = w.flops() / (ms * 1e-3) / 1e12
+    n2 = w.B * w.H * w.N * w.N
+    line = {"metric": "attention bwd TFLOP/s (recomputation)", "value": world * tflops, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": dict(w.describe(), workload=args.workload, l2="no flush between steps"),
+            "gpu_launches": 3 * args.steps,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_source": src,
+                         "kernel": "fa_bwd call (fa_bwd_pre + fa_bwd_kernel + fa_bwd_post)"},
+            "recompute": {"ms": ms, "peak_bytes_fwd_bwd": peak_ours},
+            "materialised": {"ms": mat_ms, "peak_bytes_fwd_bwd": peak_mat,
+                             "p_bytes": n2 * qd.element_size(),
+                             "path": "torch matmul/softmax with P saved in the input type"},
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(BWD_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args, DECODE_WORKLOADS[args.workload])
+    if args.workload in BWD_WORKLOADS:
+        return run_bwd(args, BWD_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

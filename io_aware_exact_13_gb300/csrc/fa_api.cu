@@ -218,6 +218,7 @@ bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
                              static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(N)};
+    // box: one 128-byte swizzle row of elements x box_rows rows x 1 head
     cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

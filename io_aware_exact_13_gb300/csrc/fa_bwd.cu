@@ -13,19 +13,30 @@
 // blocks i that can see it (all of them, or i >= j when causal):
 //   warp 0      TMA: K_j and V_j once, then Q_i and dO_i through a ring
 //   warp 1      MMA issue (warp-uniform loop, lane 0 issues), tcgen05 kind::f16
-//   warps 4-7   one thread per key (TMEM lane): P^T and dS^T from S^T, dP^T,
-//               lse and D; then one thread per query row: dQ read-out
-// Tensor memory (512 columns) per iteration:
-//   [0,128)     S^T = K_j Q_i^T  (fp32; then P^T in 16 bit in [0,64), and the
-//               dQ columns 0..63 of this block in [64,128))
-//   [128,256)   dP^T = V_j dO_i^T (fp32; then dS^T in 16 bit in [128,192), and
-//               dQ columns 64..127 in [192,256) when d = 128)
+//   warps 4-11  two warpgroups; thread r of a group owns TMEM lane r. Group g
+//               first turns query columns [64 g, 64 g + 64) of S^T, dP^T into
+//               P^T and dS^T for key r, then reads out dQ for query row r,
+//               head columns of half g, and at the end stores dV (g = 0) or
+//               dK (g = 1) of key r.
+// Tensor memory (512 columns) per iteration. Query chunk x (32 queries) has
+// its scores in S^T columns [32x, 32x+32); group 0 handles chunks 0, 1 in that
+// order, group 1 chunks 3, 2. Each group packs P^T (16 bit, two queries per
+// column) only into columns it has already read itself: chunk x goes to
+// columns 16x (x < 2) or 64 + 16x (x >= 2). So the two groups never touch each
+// other's unread scores, and columns [32,96) are free afterwards.
+//   [0,128)     S^T = K_j Q_i^T (fp32), then P^T in [0,32) and [96,128), and
+//               dQ head columns 0..63 in [32,96)
+//   [128,256)   dP^T = V_j dO_i^T (fp32), then dS^T in [128,160) and
+//               [224,256), and dQ head columns 64..127 in [160,224) (d = 128)
 //   [256,256+d) dV_j accumulator,  [256+d,256+2d) dK_j accumulator
 // dV_j += P^T dO_i and dK_j += dS^T Q_i take A from tensor memory; dQ_i = dS K_j
-// takes A = dS from shared memory, written by the key threads with the query
-// index contiguous (an M-major operand). The dQ block partials of all key
-// blocks are added with fp32 vector reductions into a workspace and converted
-// to the output type by a last kernel.
+// takes A = dS from shared memory, written by the gradient warps with the
+// query index contiguous (an M-major operand). Each warp then stages its
+// 32 x 32 fp32 tiles of dQ_i in its own part of that dS buffer and adds them
+// into an fp32 workspace with bulk tensor reductions (reduce-add in L2); a
+// last kernel converts the workspace to the output type. The row statistics
+// of block i (lse * log2 e and D, padded past N) are loaded one iteration
+// ahead and handed over in shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,7 +49,8 @@
 namespace fa {
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
+constexpr int kGradThreads = 256;  // warps 4-11
 constexpr int kBlk = kBwdRows;  // keys per CTA block and query rows per iteration
 
 template <typename T, int D>
@@ -53,8 +65,9 @@ struct BwdCfg {
     static constexpr int SMEM_V = TILE;
     static constexpr int SMEM_QD = 2 * TILE;                     // STAGES x (Q_i, dO_i)
     static constexpr int SMEM_DS = SMEM_QD + STAGES * 2 * TILE;  // dS: 2 chunks (queries 0-63, 64-127) x 128 keys
-    static constexpr int SMEM_BAR = SMEM_DS + 2 * CHUNK;
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 5;
+    static constexpr int SMEM_STATS = SMEM_DS + 2 * CHUNK;       // -lse2[128], -D[128] of the current block
+    static constexpr int SMEM_BAR = SMEM_STATS + 256 * 4;
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 6;
     static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;
     static constexpr uint32_t FMT = Elem<T>::fmt;
     static constexpr uint32_t ID_ST = make_idesc_ab(FMT, 128, 128, 0, 0);  // S^T, dP^T: A, B K-major
@@ -67,7 +80,7 @@ struct BwdCfg {
 struct BwdParams {
     const float *lse2;  // [BH][Npad]
     const float *dsum;  // [BH][Npad]
-    float *dq_acc;      // [BH][N][d]
+    float *dq_acc;      // [BH][N][d], reduced into through tm_dq
     void *dk, *dv;      // [BH][N][d]
     int *status;
     int BH, N, Npad;
@@ -105,7 +118,7 @@ template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using C = BwdCfg<T, D>;
     constexpr int ST = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -115,10 +128,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_qd_full = [&](int s) { return smem_u32(bars + 1 + s); };
     auto bar_qd_empty = [&](int s) { return smem_u32(bars + 1 + ST + s); };
     const uint32_t bar_sp_full = smem_u32(bars + 1 + 2 * ST);  // S^T, dP^T in TMEM
-    const uint32_t bar_p_full = smem_u32(bars + 2 + 2 * ST);   // P^T, dS^T, dS written (128 arrivals)
+    const uint32_t bar_p_full = smem_u32(bars + 2 + 2 * ST);   // P^T, dS^T, dS written (256 arrivals)
     const uint32_t bar_dq_full = smem_u32(bars + 3 + 2 * ST);  // every product of the iteration done
-    const uint32_t bar_dq_free = smem_u32(bars + 4 + 2 * ST);  // dQ read out (128 arrivals)
+    const uint32_t bar_dq_free = smem_u32(bars + 4 + 2 * ST);  // dQ loaded from TMEM (256 arrivals)
     const uint32_t bar_drain = smem_u32(bars + 5 + 2 * ST);    // all issued MMAs done (exit)
+    const uint32_t bar_stats = smem_u32(bars + 6 + 2 * ST);    // row statistics of the block stored (256 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,10 +151,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar_qd_empty(s), 1);
         }
         mbar_init(bar_sp_full, 1);
-        mbar_init(bar_p_full, 128);
+        mbar_init(bar_p_full, kGradThreads);
         mbar_init(bar_dq_full, 1);
-        mbar_init(bar_dq_free, 128);
+        mbar_init(bar_dq_free, kGradThreads);
         mbar_init(bar_drain, 1);
+        mbar_init(bar_stats, kGradThreads);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -216,8 +231,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int k = 0; k < C::KSTEPS_R; ++k) {
                 const uint64_t off = (uint64_t)((k * 2048) >> 4);
                 const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-                mma_ts(tmem + 256, tmem + 0 + k * 8, do_mn + off, C::ID_ACC, acc, issue);
-                mma_ts(tmem + 256 + D, tmem + 128 + k * 8, q_mn + off, C::ID_ACC, acc, issue);
+                const uint32_t pcol = (uint32_t)(k < 4 ? 8 * k : 64 + 8 * k);  // packed P^T / dS^T of queries 16k..
+                mma_ts(tmem + 256, tmem + 0 + pcol, do_mn + off, C::ID_ACC, acc, issue);
+                mma_ts(tmem + 256 + D, tmem + 128 + pcol, q_mn + off, C::ID_ACC, acc, issue);
             }
             // dQ_i = dS K_j, contracted over the 128 keys, 64 head columns at a time
 #pragma unroll
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int k = 0; k < C::KSTEPS_R; ++k) {
                     const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                    mma_ss(tmem + (h == 0 ? 64 : 192), ds_mn + off, k_mn + (uint64_t)((h * C::CHUNK) >> 4) + off,
+                    mma_ss(tmem + (h == 0 ? 32 : 160), ds_mn + off, k_mn + (uint64_t)((h * C::CHUNK) >> 4) + off,
                            C::ID_DQ, k > 0 ? 1u : 0u, issue);
                 }
             tc_commit(bar_dq_full, issue);
@@ -236,111 +252,144 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bwd_wait_warp(bar_drain, 0, p);
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- gradient warps
-        const int r = threadIdx.x - 128;  // TMEM lane: key r of block j, later query row r of block i
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int g = (warp - 4) >> 2;             // warpgroup: query columns / head columns half g
+        const int w = warp & 3;                    // TMEM lane group
+        const int r = w * 32 + lane;               // TMEM lane: key r of block j, later query row r of block i
+        const uint32_t lane_base = (uint32_t)(w * 32) << 16;
         const int key = j * kBlk + r;
         const bool key_ok = key < p.N;
-        const uint32_t ds_row = smem_u32(smem + C::SMEM_DS) + r * 128;
-        const float *lse2_bh = p.lse2 + (size_t)bh * p.Npad;
-        const float *dsum_bh = p.dsum + (size_t)bh * p.Npad;
+        const uint32_t ds_base = smem_u32(smem + C::SMEM_DS);
+        const uint32_t stats = smem_u32(smem + C::SMEM_STATS);
+        // this warp's 4 KB of the dS buffer (its 32 key rows of chunk g), reused to stage dQ tiles
+        const uint32_t stage = ds_base + g * C::CHUNK + w * 4096;
+        // one statistic per thread: -lse2 (group 0) or -D (group 1) of query row r of the block
+        const float *stat_src = (g == 0 ? p.lse2 : p.dsum) + (size_t)bh * p.Npad + r;
+        float stat_next = -__ldg(stat_src + i0 * kBlk);
+        const bool ragged_keys = (j + 1) * kBlk > p.N;
         bool ok = true;
         for (int it = 0; ok && it < n_it; ++it) {
-            const int row0 = (i0 + it) * kBlk;
-            ok = bwd_wait_warp(bar_sp_full, it & 1u, p);
+            const int i = i0 + it;
+            const int row0 = i * kBlk;
+            // hand over the block's statistics (their last readers passed p_full of the previous block)
+            st_shared_f32(stats + (g * 128 + r) * 4, stat_next);
+            mbar_arrive(bar_stats);
+            ok = bwd_wait_warp(bar_stats, it & 1u, p) && bwd_wait_warp(bar_sp_full, it & 1u, p);
             if (!ok) break;
             tc_fence_after();
+            const bool need_mask = ragged_keys || (CAUSAL && i == j);
 #pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {  // 32 query rows (TMEM columns) at a time
-                float4 l4[8], d4[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {  // same address across the warp: broadcast loads
-                    l4[u] = ld_global_nc_v4(lse2_bh + row0 + c0 + 4 * u);
-                    d4[u] = ld_global_nc_v4(dsum_bh + row0 + c0 + 4 * u);
-                }
+            for (int step = 0; step < 2; ++step) {  // 32 query rows (TMEM columns) at a time
+                const int c0 = g == 0 ? 32 * step : 96 - 32 * step;
+                const uint32_t pcol = (uint32_t)(c0 < 64 ? c0 / 2 : 64 + c0 / 2);  // packed P^T / dS^T column
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_wait(tmem + lane_base + c0, sv, tmem + lane_base + 128 + c0, dpv);
-                const float *lf = reinterpret_cast<const float *>(l4);
-                const float *df = reinterpret_cast<const float *>(d4);
                 uint32_t pp[16], dsp[16];
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float pr[2], dsr[2];
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 nl = ld_shared_v4f(stats + (c0 + c) * 4);        // -lse2, same for the warp
+                    const float4 nd = ld_shared_v4f(stats + (128 + c0 + c) * 4);  // -D
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        bool vis = key_ok;
-                        if (CAUSAL) vis = vis && (key <= row0 + c0 + c + u);
-                        const float x = fmaf(__uint_as_float(sv[c + u]), p.scale_log2, -lf[c + u]);
-                        const float pe = vis ? ex2_approx(x) : 0.0f;
-                        pr[u] = pe;
-                        dsr[u] = pe * (__uint_as_float(dpv[c + u]) - df[c + u]);
+                    for (int h = 0; h < 4; h += 2) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(sv[c + h]), __uint_as_float(sv[c + h + 1])),
+                                               make_float2(p.scale_log2, p.scale_log2),
+                                               h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
+                        float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        if (need_mask) {
+                            const int q0 = row0 + c0 + c + h;
+                            const bool v0 = key_ok && (!CAUSAL || key <= q0);
+                            const bool v1 = key_ok && (!CAUSAL || key <= q0 + 1);
+                            pe.x = v0 ? pe.x : 0.0f;
+                            pe.y = v1 ? pe.y : 0.0f;
+                        }
+                        const float2 t = fadd2(make_float2(__uint_as_float(dpv[c + h]), __uint_as_float(dpv[c + h + 1])),
+                                               h == 0 ? make_float2(nd.x, nd.y) : make_float2(nd.z, nd.w));
+                        const float2 ds = fmul2(pe, t);
+                        pp[(c + h) / 2] = pk2<T>(pe.x, pe.y);
+                        dsp[(c + h) / 2] = pk2<T>(ds.x, ds.y);
                     }
-                    pp[c / 2] = pk2<T>(pr[0], pr[1]);
-                    dsp[c / 2] = pk2<T>(dsr[0], dsr[1]);
                 }
-                // P^T and dS^T overwrite columns this thread has already read.
-                tmem_st16(tmem + lane_base + 0 + c0 / 2, pp);
-                tmem_st16(tmem + lane_base + 128 + c0 / 2, dsp);
-                // dS row of key r: queries c0..c0+31 = 64 bytes of chunk c0/64, 128-byte swizzle
+                // P^T and dS^T overwrite columns this warpgroup has already read.
+                tmem_st16(tmem + lane_base + 0 + pcol, pp);
+                tmem_st16(tmem + lane_base + 128 + pcol, dsp);
+                // dS row of key r: queries c0..c0+31 = 64 bytes of chunk g, 128-byte swizzle
+                const uint32_t ds_row = ds_base + g * C::CHUNK + r * 128;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t unit = (uint32_t)(((c0 % 64) / 8 + u) ^ (r & 7));
-                    st_shared_v4(ds_row + (c0 / 64) * C::CHUNK + unit * 16, dsp[4 * u], dsp[4 * u + 1],
-                                 dsp[4 * u + 2], dsp[4 * u + 3]);
+                    st_shared_v4(ds_row + unit * 16, dsp[4 * u], dsp[4 * u + 1], dsp[4 * u + 2], dsp[4 * u + 3]);
                 }
             }
             tmem_wait_st();
             fence_proxy_async_smem();  // dS is read by the tensor core (async proxy)
             tc_fence_before();
             mbar_arrive(bar_p_full);
-            // dQ_i rows (TMEM lane = query row r): scale and add into the fp32 accumulator
+            if (it + 1 < n_it) stat_next = -__ldg(stat_src + (i + 1) * kBlk);  // in flight during the read-out
+            // dQ_i rows 32w..32w+31, head columns of half g: load them, release the
+            // tensor memory at once (the next block's S^T, dP^T may then be computed),
+            // then stage 32 x 32 fp32 tiles and reduce-add them into the workspace.
             ok = bwd_wait_warp(bar_dq_full, it & 1u, p);
             if (!ok) break;
             tc_fence_after();
-            const int row = row0 + r;
-            float *dq_row = p.dq_acc + ((size_t)bh * p.N + (size_t)(row < p.N ? row : 0)) * D;
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint32_t qa[32], qb[32];
-                const uint32_t col = h == 0 ? 64u : 192u;
-                tmem_ld32x2_wait(tmem + lane_base + col, qa, tmem + lane_base + col + 32, qb);
-                if (row < p.N) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        red_add_v4(dq_row + h * 64 + c, __uint_as_float(qa[c]) * p.scale,
-                                   __uint_as_float(qa[c + 1]) * p.scale, __uint_as_float(qa[c + 2]) * p.scale,
-                                   __uint_as_float(qa[c + 3]) * p.scale);
-                        red_add_v4(dq_row + h * 64 + 32 + c, __uint_as_float(qb[c]) * p.scale,
-                                   __uint_as_float(qb[c + 1]) * p.scale, __uint_as_float(qb[c + 2]) * p.scale,
-                                   __uint_as_float(qb[c + 3]) * p.scale);
-                    }
-                }
+            constexpr int COLS = D / 2;  // head columns per warpgroup (32 or 64)
+            const uint32_t qcol = (D == 64) ? (32u + 32u * g) : (g == 0 ? 32u : 160u);
+            uint32_t qv[COLS];
+            if constexpr (COLS == 32) {
+                tmem_ld32_wait(tmem + lane_base + qcol, *reinterpret_cast<uint32_t(*)[32]>(qv));
+            } else {
+                tmem_ld32x2_wait(tmem + lane_base + qcol, *reinterpret_cast<uint32_t(*)[32]>(qv),
+                                 tmem + lane_base + qcol + 32, *reinterpret_cast<uint32_t(*)[32]>(qv + 32));
             }
             tc_fence_before();
             mbar_arrive(bar_dq_free);
+#pragma unroll
+            for (int t = 0; t < COLS / 32; ++t) {
+                if (t > 0) {  // the previous tile's reduction must have read the staging area
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) * 16),
+                                 __float_as_uint(__uint_as_float(qv[32 * t + 4 * u]) * p.scale),
+                                 __float_as_uint(__uint_as_float(qv[32 * t + 4 * u + 1]) * p.scale),
+                                 __float_as_uint(__uint_as_float(qv[32 * t + 4 * u + 2]) * p.scale),
+                                 __float_as_uint(__uint_as_float(qv[32 * t + 4 * u + 3]) * p.scale));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_3d(&tm_dq, stage, g * COLS + 32 * t, row0 + w * 32, bh);
+                    bulk_commit_group();
+                }
+            }
+            // the staging area is this warp's dS rows: free it before the next block writes dS
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
         }
-        // ---------------------------------------------------------------- dK_j, dV_j
+        if (lane == 0) bulk_wait_all();
+        // ---------------------------------------------------------------- dV_j (group 0), dK_j (group 1)
         // The last dq_full completion covers every dV and dK product (a commit
         // tracks all earlier MMAs of the issuing thread).
         if (ok) {
             tc_fence_after();
-            T *dv_row = reinterpret_cast<T *>(p.dv) + ((size_t)bh * p.N + (size_t)(key_ok ? key : 0)) * D;
-            T *dk_row = reinterpret_cast<T *>(p.dk) + ((size_t)bh * p.N + (size_t)(key_ok ? key : 0)) * D;
+            const float mul = g == 0 ? 1.0f : p.scale;
+            T *dst = reinterpret_cast<T *>(g == 0 ? p.dv : p.dk) + ((size_t)bh * p.N + (size_t)(key_ok ? key : 0)) * D;
+            const uint32_t src_col = 256u + (uint32_t)(g * D);
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 64) {
                 uint32_t a[32], b[32];
-                tmem_ld32x2_wait(tmem + lane_base + 256 + c0, a, tmem + lane_base + 256 + D + c0, b);
+                tmem_ld32x2_wait(tmem + lane_base + src_col + c0, a, tmem + lane_base + src_col + c0 + 32, b);
                 if (key_ok) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
-                        st_global_v4(dv_row + c0 + c, pk2<T>(__uint_as_float(a[c]), __uint_as_float(a[c + 1])),
-                                     pk2<T>(__uint_as_float(a[c + 2]), __uint_as_float(a[c + 3])),
-                                     pk2<T>(__uint_as_float(a[c + 4]), __uint_as_float(a[c + 5])),
-                                     pk2<T>(__uint_as_float(a[c + 6]), __uint_as_float(a[c + 7])));
-                        st_global_v4(dk_row + c0 + c,
-                                     pk2<T>(__uint_as_float(b[c]) * p.scale, __uint_as_float(b[c + 1]) * p.scale),
-                                     pk2<T>(__uint_as_float(b[c + 2]) * p.scale, __uint_as_float(b[c + 3]) * p.scale),
-                                     pk2<T>(__uint_as_float(b[c + 4]) * p.scale, __uint_as_float(b[c + 5]) * p.scale),
-                                     pk2<T>(__uint_as_float(b[c + 6]) * p.scale, __uint_as_float(b[c + 7]) * p.scale));
+                        st_global_v4(dst + c0 + c, pk2<T>(__uint_as_float(a[c]) * mul, __uint_as_float(a[c + 1]) * mul),
+                                     pk2<T>(__uint_as_float(a[c + 2]) * mul, __uint_as_float(a[c + 3]) * mul),
+                                     pk2<T>(__uint_as_float(a[c + 4]) * mul, __uint_as_float(a[c + 5]) * mul),
+                                     pk2<T>(__uint_as_float(a[c + 6]) * mul, __uint_as_float(a[c + 7]) * mul));
+                        st_global_v4(dst + c0 + 32 + c,
+                                     pk2<T>(__uint_as_float(b[c]) * mul, __uint_as_float(b[c + 1]) * mul),
+                                     pk2<T>(__uint_as_float(b[c + 2]) * mul, __uint_as_float(b[c + 3]) * mul),
+                                     pk2<T>(__uint_as_float(b[c + 4]) * mul, __uint_as_float(b[c + 5]) * mul),
+                                     pk2<T>(__uint_as_float(b[c + 6]) * mul, __uint_as_float(b[c + 7]) * mul));
                     }
                 }
             }
@@ -427,6 +476,8 @@ int launch_bwd_variant(const BwdArgs &a) {
     if (!encode_rows_map(&tk, Elem<T>::tma, 2, a.k, D, a.N, BH, kBlk)) return -5;
     if (!encode_rows_map(&tv, Elem<T>::tma, 2, a.v, D, a.N, BH, kBlk)) return -5;
     if (!encode_rows_map(&tdo, Elem<T>::tma, 2, a.dout, D, a.N, BH, kBlk)) return -5;
+    CUtensorMap tdq;  // fp32 dQ accumulator, 32 x 32 boxes (128-byte rows), reduced into
+    if (!encode_rows_map(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dq_acc, D, a.N, BH, 32)) return -5;
     BwdParams p;
     p.lse2 = a.lse2;
     p.dsum = a.dsum;
@@ -441,7 +492,7 @@ int launch_bwd_variant(const BwdArgs &a) {
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
     const int64_t grid = static_cast<int64_t>(BH) * (Npad / kBlk);
-    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, p);
+    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
     const size_t n4 = static_cast<size_t>(BH) * a.N * D / 4;
     fa_bwd_post<T><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dq_acc, static_cast<T *>(a.dq),

@@ -194,12 +194,15 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
     return True
 
 
-def simulate_bwd(n_it, stages, seed, key_warps=4):
+def simulate_bwd(n_it, stages, seed, grad_warps=8):
     """The backward kernel's protocol for one CTA (one key block visiting n_it
-    query blocks): TMA producer, MMA issuer, and the key/row warps."""
+    query blocks): TMA producer, MMA issuer, and the gradient warps (two
+    warpgroups, 256 arrivals per phase on their barriers)."""
     rnd = random.Random(seed)
     B = {}
-    for name, c in (("kv", 1), ("sp_full", 1), ("p_full", BQ), ("dq_full", 1), ("dq_free", BQ), ("drain", 1)):
+    n = 32 * grad_warps
+    for name, c in (("kv", 1), ("sp_full", 1), ("p_full", n), ("dq_full", 1), ("dq_free", n), ("drain", 1),
+                    ("stats", n)):
         B[name] = Bar(name, c)
     for s in range(stages):
         B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
@@ -226,16 +229,18 @@ def simulate_bwd(n_it, stages, seed, key_warps=4):
         tensor_pipe.append(("commit", "drain"))
         yield ("wait", "drain", 0)
 
-    def keys():
+    def grads():
         for it in range(n_it):
+            yield ("arrive", "stats", 32)  # statistics of block it stored (their readers passed p_full(it-1))
+            yield ("wait", "stats", it)
             yield ("wait", "sp_full", it)
-            yield ("arrive", "p_full", BQ // key_warps)
+            yield ("arrive", "p_full", 32)
             yield ("wait", "dq_full", it)
-            yield ("arrive", "dq_free", BQ // key_warps)
+            yield ("arrive", "dq_free", 32)
 
     agents = {"producer": producer(), "mma": mma()}
-    for w in range(key_warps):
-        agents[f"keys{w}"] = keys()
+    for w in range(grad_warps):
+        agents[f"grads{w}"] = grads()
     waiting = {k: None for k in agents}
     while agents or tensor_pipe or tma:
         ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
