@@ -39,8 +39,9 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, HEADLINE, WORKLOADS,  # noqa: E402
-                                            make_bwd, make_decode, make_workload, sample_rows)
+from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, HEADLINE, VARLEN_WORKLOADS,  # noqa: E402
+                                            WORKLOADS, make_bwd, make_decode, make_varlen, make_workload,
+                                            sample_rows)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
 UNIT = "TFLOP/s"
@@ -391,6 +392,60 @@ def run_decode(args, w):
     return 0
 
 
+def run_varlen(args, w):
+    """Packed variable-length batch through the persistent forward kernel."""
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from io_aware_exact_13_gb300 import fa
+
+    L = w.lengths()
+    q, k, v, cu = make_varlen(L, w.H, w.H, w.d, w.dtype, seed=w.seed)
+    qd, kd, vd, cud = q.to(dev), k.to(dev), v.to(dev), cu.to(dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    entry = fa.fa_fwd_varlen if w.dtype == "bf16" else fa.fa_fwd_varlen_fp16
+
+    def step():
+        entry(qd, kd, vd, od, lsed, cud, max(L), w.scale, w.causal, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status(stream) != 0:
+        raise SystemExit("device status word set during warm-up")
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world, dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(world, a.elapsed_time(b), dev) / args.steps
+    if rank != 0:
+        return 0
+    peak, src = load_peak()
+    tflops = w.flops() / (ms * 1e-3) / 1e12
+    line = {"metric": "attention fwd TFLOP/s, packed variable-length batch", "value": world * tflops,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(w.describe(), workload=args.workload, l2="no flush between steps"),
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_source": src,
+                         "kernel": "fa_fwd_kernel (packed batch)"},
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def materialised_backward(q, k, v, dout, scale, causal):
     """The stored-state comparison path of the backward measurement, in plain
     torch ops: S and P are materialised ([B,H,N,N]) by the forward and P is
@@ -519,7 +574,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(BWD_WORKLOADS))
+                    choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(BWD_WORKLOADS)
+                    + sorted(VARLEN_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -528,6 +584,8 @@ def main():
         return run_decode(args, DECODE_WORKLOADS[args.workload])
     if args.workload in BWD_WORKLOADS:
         return run_bwd(args, BWD_WORKLOADS[args.workload])
+    if args.workload in VARLEN_WORKLOADS:
+        return run_varlen(args, VARLEN_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -52,7 +52,8 @@ typedef enum {
     FA_ERR_UNSUPPORTED = -4, /* d not supported for this element type */
     FA_ERR_LAUNCH = -5,      /* the CUDA launch (or tensor-map encoding) failed */
     FA_ERR_TIMEOUT = -6,     /* a device-side wait gave up (device status word) */
-    FA_ERR_WORKSPACE = -7    /* workspace missing or smaller than the problem needs */
+    FA_ERR_WORKSPACE = -7,   /* workspace missing or smaller than the problem needs */
+    FA_ERR_SEQLENS = -8      /* packed batch: cu_seqlens inconsistent (device status word) */
 } fa_status;
 
 /* bf16 Q/K/V/out, fp32 accumulation. d in {64, 128}. */
@@ -127,6 +128,30 @@ int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, 
 int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
                            int Nq, int Nk, int d, float scale, int causal, int n_splits, void *stream);
 
+/* ---- packed variable-length batch ------------------------------------------
+ * The same attention for nseq independent sequences packed back to back
+ * ("IO-aware exact attention", section "Tile order and on-chip capacity":
+ * packed sequences add bounds and indexing). Sequence s holds tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]) and attends only within itself; causal
+ * allows key j for query i of the same sequence iff j <= i.
+ * Layouts (DEVICE pointers, token-major, last index fastest):
+ *   q, out : [total][H][d]      k, v : [total][Hkv][d]      lse : float [H][total]
+ *   cu_seqlens : int32 [nseq + 1], cu_seqlens[0] = 0, non-decreasing,
+ *                cu_seqlens[nseq] <= total (tokens past it are left untouched).
+ * max_seqlen is a host-side upper bound on every sequence length; work is
+ * sized by nseq * H * ceil(max_seqlen / 256). The bounds are read on the
+ * device: a sequence with cu_seqlens[s+1] < cu_seqlens[s], a negative start,
+ * an end past total or a length above max_seqlen is skipped (its rows are not
+ * written) and FA_ERR_SEQLENS is recorded in the device status word. A
+ * zero-length sequence is allowed. Hkv must divide H (grouped-query attention
+ * as in fa_fwd_gqa). No mask argument. d in {64, 128}. */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse, const int *cu_seqlens,
+                  int nseq, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                  void *stream);
+int fa_fwd_varlen_fp16(const void *q, const void *k, const void *v, void *out, float *lse, const int *cu_seqlens,
+                       int nseq, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                       void *stream);
+
 /* ---- backward by recomputation ---------------------------------------------
  * Gradients of L = sum(dout o out) for out = softmax(scale Q K^T) V ("IO-aware
  * exact attention", section "Backward recomputation"): from q, k, v, the
@@ -159,7 +184,7 @@ int fa_bwd_fp16(const void *q, const void *k, const void *v, const void *out, co
 const char *fa_status_string(int status);
 
 /* Synchronises `stream`, returns the device status word of the current device
- * (FA_OK or FA_ERR_TIMEOUT) and clears it. Returns FA_ERR_LAUNCH if the
+ * (FA_OK, FA_ERR_TIMEOUT or FA_ERR_SEQLENS) and clears it. Returns FA_ERR_LAUNCH if the
  * synchronisation itself fails. */
 int fa_get_device_status(void *stream);
 

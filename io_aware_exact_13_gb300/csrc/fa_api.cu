@@ -17,6 +17,8 @@ namespace fa {
 int launch_fwd_bf16(const LaunchArgs &a);
 int launch_fwd_fp16(const LaunchArgs &a);
 int launch_fwd_fp32(const LaunchArgs &a);
+int launch_fwd_varlen_bf16(const LaunchArgs &a);
+int launch_fwd_varlen_fp16(const LaunchArgs &a);
 }  // namespace fa
 
 // Device status word: FA_OK, or FA_ERR_TIMEOUT once any bounded wait gave up.
@@ -162,6 +164,43 @@ int splitkv_common(bool fp16, const void *q, const void *k, const void *v, void 
     return fa::launch_splitkv(a, fp16);
 }
 
+int varlen_common(bool fp16, const void *q, const void *k, const void *v, void *out, float *lse,
+                  const int *cu_seqlens, int nseq, int total, int max_seqlen, int H, int Hkv, int d, float scale,
+                  int causal, void *stream) {
+    if (!q || !k || !v || !out || !lse || !cu_seqlens) return FA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens, 4))
+        return FA_ERR_ALIGN;
+    if (nseq < 1 || total < 1 || max_seqlen < 1 || H < 1 || Hkv < 1 || H % Hkv != 0) return FA_ERR_SHAPE;
+    const int64_t items = static_cast<int64_t>(nseq) * H * ((static_cast<int64_t>(max_seqlen) + 255) / 256);
+    if (items > INT32_MAX) return FA_ERR_SHAPE;
+    if (static_cast<int64_t>(H) * total > INT32_MAX) return FA_ERR_SHAPE;  // lse index
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    DeviceInfo *di = device_info();
+    if (!di || !encoder()) return FA_ERR_LAUNCH;
+    fa::LaunchArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.mask = nullptr;
+    a.out = out;
+    a.lse = lse;
+    a.B = nseq;
+    a.H = H;
+    a.N = max_seqlen;
+    a.d = d;
+    a.Hkv = Hkv;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status = di->status;
+    a.num_sms = di->num_sms;
+    a.timeout_ns = kDefaultTimeoutNs;
+    a.cu_seqlens = cu_seqlens;
+    a.total = total;
+    return fp16 ? fa::launch_fwd_varlen_fp16(a) : fa::launch_fwd_varlen_bf16(a);
+}
+
 int bwd_common(bool fp16, const void *q, const void *k, const void *v, const void *out, const void *dout,
                const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
                void *workspace, unsigned long long workspace_bytes, void *stream) {
@@ -220,6 +259,22 @@ bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes
                              static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(N)};
     // box: one 128-byte swizzle row of elements x box_rows rows x 1 head
     cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_tokens_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d,
+                       int heads, int total, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes,
+                             static_cast<cuuint64_t>(d) * elem_bytes * static_cast<cuuint64_t>(heads)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -292,6 +347,19 @@ int fa_fwd_gqa_fp16(const void *q, const void *k, const void *v, const float *ma
     return fwd_common(Type::FP16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream, Hkv);
 }
 
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse, const int *cu_seqlens,
+                  int nseq, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal, void *stream) {
+    return varlen_common(false, q, k, v, out, lse, cu_seqlens, nseq, total, max_seqlen, H, Hkv, d, scale, causal,
+                         stream);
+}
+
+int fa_fwd_varlen_fp16(const void *q, const void *k, const void *v, void *out, float *lse, const int *cu_seqlens,
+                       int nseq, int total, int max_seqlen, int H, int Hkv, int d, float scale, int causal,
+                       void *stream) {
+    return varlen_common(true, q, k, v, out, lse, cu_seqlens, nseq, total, max_seqlen, H, Hkv, d, scale, causal,
+                         stream);
+}
+
 long long fa_bwd_workspace_bytes(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -322,6 +390,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_LAUNCH: return "CUDA launch or tensor-map encoding failed";
         case FA_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
         case FA_ERR_WORKSPACE: return "workspace missing or smaller than the problem needs";
+        case FA_ERR_SEQLENS: return "cu_seqlens inconsistent with total or max_seqlen (device status)";
         default: return "unknown status";
     }
 }

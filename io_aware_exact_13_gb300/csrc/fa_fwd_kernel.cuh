@@ -58,6 +58,7 @@ constexpr int kRowsPerItem = 256;  // two query tiles per work item
 constexpr int kThreads = 512;
 constexpr float kTau = 8.0f;       // lazy-rescale threshold, log2 units
 constexpr int kStatusTimeout = -6; // value written to the device status word
+constexpr int kStatusSeqlens = -8; // packed batch: cu_seqlens inconsistent with total / max_seqlen
 
 template <typename T>
 struct Elem;
@@ -116,6 +117,10 @@ struct FwdParams {
     int n_kv;           // ceil(N / 64)
     float scale_log2;   // scale * log2(e)
     uint64_t timeout_ns;
+    // packed variable-length batch (B = number of sequences, N = max_seqlen):
+    const int *cu_seqlens;  // [B + 1] token offsets of the sequences
+    int total;              // tokens in the batch
+    int Hkv;                // key/value heads
 };
 
 // Static schedule: CTA c takes item w*G + c in even waves w and w*G + (G-1-c)
@@ -138,13 +143,38 @@ __device__ __forceinline__ void item_coords(const FwdParams &p, int item, int &b
     q0 = qb * kRowsPerItem;
 }
 
-// Number of K/V blocks query tile t of an item at q0 must visit.
+// One work item as every role sees it: head row bh (= b*H + h), first query row
+// q0 within its sequence, the sequence length n and, in a packed batch, the
+// token index of the sequence's first row.
+struct Item {
+    int bh, q0, n, tok0;
+};
+
+template <bool VARLEN>
+__device__ __forceinline__ Item get_item(const FwdParams &p, int item) {
+    Item it;
+    item_coords(p, item, it.bh, it.q0);
+    it.n = p.N;
+    it.tok0 = 0;
+    if constexpr (VARLEN) {
+        const int s = it.bh / p.H;
+        const int a = __ldg(p.cu_seqlens + s), b = __ldg(p.cu_seqlens + s + 1);
+        // a sequence whose bounds do not fit the batch is skipped (and reported once)
+        const bool bad = a < 0 || b < a || b > p.total || b - a > p.N;
+        if (bad && it.q0 == 0 && (it.bh % p.H) == 0 && threadIdx.x == 0) atomicExch(p.status, kStatusSeqlens);
+        it.n = bad ? 0 : b - a;
+        it.tok0 = bad ? 0 : a;
+    }
+    return it;
+}
+
+// Number of K/V blocks query tile t of an item must visit.
 template <bool CAUSAL>
-__device__ __forceinline__ int tile_nkv(const FwdParams &p, int q0, int t) {
-    const int r0 = q0 + t * kBQ;
-    if (r0 >= p.N) return 0;
-    if (!CAUSAL) return p.n_kv;
-    const int last_row = min(p.N, r0 + kBQ) - 1;
+__device__ __forceinline__ int tile_nkv(const Item &it, int t) {
+    const int r0 = it.q0 + t * kBQ;
+    if (r0 >= it.n) return 0;
+    if (!CAUSAL) return (it.n + kBK - 1) / kBK;
+    const int last_row = min(it.n, r0 + kBQ) - 1;
     return last_row / kBK + 1;
 }
 
@@ -206,10 +236,14 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <typename T, int D, bool CAUSAL, bool HAS_MASK>
+// VARLEN: q, out are [total][H][d] and k, v [total][Hkv][d] (token-major, packed
+// sequences); their tensor maps are (d, heads, total) with 1 x 128 / 1 x 64 boxes,
+// so a tile lands in shared memory exactly as in the [B][H][N][d] case.
+template <typename T, int D, bool CAUSAL, bool HAS_MASK, bool VARLEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    static_assert(!(VARLEN && HAS_MASK), "no mask in a packed batch");
     using C = Cfg<T, D>;
     constexpr int R = C::RING;
     extern __shared__ uint8_t smem_raw[];
@@ -268,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_q = policy_evict_first();
             uint32_t qcount[2] = {0, 0};
             uint32_t kpos = 0, vpos = 0;
-            int cur_bh = 0, kv_bh = 0;
+            int kv_y = 0, kv_z = 0, tok0 = 0;  // K/V tensor-map coordinates of the item
             bool ok = true;
             auto load_kv = [&](bool is_v, int blk) -> bool {
                 uint32_t &pos = is_v ? vpos : kpos;
@@ -281,19 +315,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(full, C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::NCH; ++c)
-                        tma_load_3d(dst + c * C::KV_CHUNK, is_v ? &tm_v : &tm_k, full, c * C::CHUNK_ELEMS, blk * kBK,
-                                    kv_bh, pol_kv);
+                        tma_load_3d(dst + c * C::KV_CHUNK, is_v ? &tm_v : &tm_k, full, c * C::CHUNK_ELEMS,
+                                    VARLEN ? kv_y : blk * kBK, VARLEN ? tok0 + blk * kBK : kv_z, pol_kv);
                 }
                 __syncwarp();
                 ++pos;
                 return true;
             };
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                int q0;
-                item_coords(p, item, cur_bh, q0);
+                const Item itm = get_item<VARLEN>(p, item);
+                const int q0 = itm.q0, cur_bh = itm.bh;
                 // grouped-query attention: kv_group consecutive query heads share one K/V head
-                kv_bh = (cur_bh / p.H) * (p.H / p.kv_group) + (cur_bh % p.H) / p.kv_group;
-                const int n0 = tile_nkv<CAUSAL>(p, q0, 0), n1 = tile_nkv<CAUSAL>(p, q0, 1);
+                const int kv_h = (cur_bh % p.H) / p.kv_group;
+                if (VARLEN) {
+                    kv_y = kv_h;
+                    tok0 = itm.tok0;
+                } else {
+                    kv_z = (cur_bh / p.H) * (p.H / p.kv_group) + kv_h;
+                }
+                const int n0 = tile_nkv<CAUSAL>(itm, 0), n1 = tile_nkv<CAUSAL>(itm, 1);
                 const int nmax = max(n0, n1);
                 for (int t = 0; t < 2 && ok; ++t) {
                     if ((t == 0 ? n0 : n1) == 0) continue;
@@ -304,13 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(sy.q_full(t), C::Q_TILE);
 #pragma unroll
                         for (int c = 0; c < C::NCH; ++c)
-                            tma_load_3d(dst + c * C::Q_CHUNK, &tm_q, sy.q_full(t), c * C::CHUNK_ELEMS, q0 + t * kBQ,
-                                        cur_bh, pol_q);
+                            tma_load_3d(dst + c * C::Q_CHUNK, &tm_q, sy.q_full(t), c * C::CHUNK_ELEMS,
+                                        VARLEN ? cur_bh % p.H : q0 + t * kBQ,
+                                        VARLEN ? tok0 + q0 + t * kBQ : cur_bh, pol_q);
                     }
                     __syncwarp();
                     ++qcount[t];
                 }
-                if (ok) ok = load_kv(false, 0);
+                // an item with no rows (a packed sequence shorter than q0) loads nothing:
+                // every K/V slot filled here must be consumed by the issuers
+                if (ok && nmax > 0) ok = load_kv(false, 0);
                 for (int j = 0; ok && j < nmax; ++j) {
                     if (j + 1 < nmax) ok = load_kv(false, j + 1);
                     if (ok) ok = load_kv(true, j);
@@ -344,10 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t qcount = 0, s_issued = 0, kpos = 0;
             bool ok = true;
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                int bh, q0;
-                item_coords(p, item, bh, q0);
-                const int nt = tile_nkv<CAUSAL>(p, q0, t);
-                const int nmax = max(tile_nkv<CAUSAL>(p, q0, 0), tile_nkv<CAUSAL>(p, q0, 1));
+                const Item itm = get_item<VARLEN>(p, item);
+                const int nt = tile_nkv<CAUSAL>(itm, t);
+                const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
                 if (nt > 0) {
                     ok = wait_warp(sy.q_full(t), qcount & 1u, abort_flag, p);
                     ++qcount;
@@ -390,10 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t g = 0, vpos = 0;
             bool ok = true;
             for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                int bh, q0;
-                item_coords(p, item, bh, q0);
-                const int nt = tile_nkv<CAUSAL>(p, q0, t);
-                const int nmax = max(tile_nkv<CAUSAL>(p, q0, 0), tile_nkv<CAUSAL>(p, q0, 1));
+                const Item itm = get_item<VARLEN>(p, item);
+                const int nt = tile_nkv<CAUSAL>(itm, t);
+                const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
                 for (int j = 0; ok && j < nmax; ++j, ++vpos) {
                     const int slot = vpos % R;
                     ok = wait_warp(sy.v_full(slot), (vpos / R) & 1u, abort_flag, p);
@@ -438,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
         bool ok = true;
         for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-            int bh, q0;
-            item_coords(p, item, bh, q0);
-            const int nt = tile_nkv<CAUSAL>(p, q0, t);
+            const Item itm = get_item<VARLEN>(p, item);
+            const int bh = itm.bh, q0 = itm.q0, n = itm.n;
+            const int nt = tile_nkv<CAUSAL>(itm, t);
             if (nt == 0) continue;
             const int row = q0 + t * kBQ + r;  // global query row (may be >= N in a ragged tail)
             const int b = bh / p.H;
@@ -486,10 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // keys past the end of the sequence, and (causal) keys after the query
                 const int tile_row0 = q0 + t * kBQ;
-                const bool ragged = kbase + kBK > p.N;
+                const bool ragged = kbase + kBK > n;
                 const bool diag = CAUSAL && (kbase + kBK - 1 > tile_row0);
                 if (ragged || diag) {
-                    int lim = p.N - 1 - kbase;
+                    int lim = n - 1 - kbase;
                     if (CAUSAL) lim = min(lim, row - kbase);
 #pragma unroll
                     for (int c = 0; c < 64; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
@@ -561,12 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-            T *orow = reinterpret_cast<T *>(p.out) + ((size_t)bh * p.N + (size_t)row) * D;
+            // [B][H][N][d] rows, or token-major [total][H][d] rows of a packed batch
+            const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
+                                           : ((size_t)bh * p.N + (size_t)row);
+            T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t ov[32];
                 tmem_ld32_wait(o_addr + c0, ov);
-                if (row < p.N) {
+                if (row < n) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 8)
                         st_global_v4(orow + c0 + c,
@@ -576,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      pack2<T>(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv));
                 }
             }
-            if (row < p.N)
-                p.lse[(size_t)bh * p.N + row] =
+            if (row < n)  // lse: [B][H][N], or [H][total] for a packed batch
+                p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
                     (l > 0.0f) ? (m_ref + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
         }
     }

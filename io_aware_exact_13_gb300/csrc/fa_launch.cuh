@@ -22,12 +22,20 @@ struct LaunchArgs {
     int *status;      // device status word
     int num_sms;
     uint64_t timeout_ns;
+    // packed variable-length batch (B = number of sequences, N = max_seqlen)
+    const int *cu_seqlens = nullptr;
+    int total = 0;
 };
 
 // Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with box_rows-row x
 // 128-byte boxes and 128-byte swizzle. Returns false on failure.
 bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d, int N,
                      int BH, int box_rows);
+// Defined in fa_api.cu: encodes a token-major [total][heads][d] tensor as the
+// 3-D map (d, heads, total) with 128-byte x 1 head x box_rows-token boxes and
+// 128-byte swizzle. Returns false on failure.
+bool encode_tokens_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d,
+                       int heads, int total, int box_rows);
 
 template <typename T, int D, bool CAUSAL, bool MASK>
 int launch_variant(const LaunchArgs &a) {
@@ -60,9 +68,52 @@ int launch_variant(const LaunchArgs &a) {
     p.n_items = BH * p.n_qblk;
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
+    p.cu_seqlens = nullptr;
+    p.total = 0;
+    p.Hkv = a.Hkv;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+template <typename T, int D, bool CAUSAL>
+int launch_varlen_variant(const LaunchArgs &a) {
+    using C = Cfg<T, D>;
+    auto kern = fa_fwd_kernel<T, D, CAUSAL, false, true>;
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
+    if (attr.numRegs * kThreads < 256 * 200 + 256 * 56) return -5;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return -5;
+    CUtensorMap tq, tk, tv;
+    if (!encode_tokens_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.H, a.total, kBQ)) return -5;
+    if (!encode_tokens_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.Hkv, a.total, kBK)) return -5;
+    if (!encode_tokens_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.Hkv, a.total, kBK)) return -5;
+    FwdParams p;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.mask = nullptr;
+    p.status = a.status;
+    p.B = a.B;
+    p.H = a.H;
+    p.kv_group = a.H / a.Hkv;
+    p.N = a.N;  // max_seqlen
+    p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
+    p.n_kv = (a.N + kBK - 1) / kBK;
+    p.n_items = a.B * a.H * p.n_qblk;
+    p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+    p.timeout_ns = a.timeout_ns;
+    p.cu_seqlens = a.cu_seqlens;
+    p.total = a.total;
+    p.Hkv = a.Hkv;
+    const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+template <typename T, int D>
+int launch_varlen_d(const LaunchArgs &a) {
+    return a.causal ? launch_varlen_variant<T, D, true>(a) : launch_varlen_variant<T, D, false>(a);
 }
 
 template <typename T, int D>

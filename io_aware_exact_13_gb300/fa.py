@@ -7,9 +7,10 @@ has not been built, and every call raises if the library returns an error.
 
 Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
 ``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), ``fa_bwd`` /
-``fa_bwd_fp16`` (backward by recomputation), their sizing helpers,
+``fa_bwd_fp16`` (backward by recomputation), ``fa_fwd_varlen`` /
+``fa_fwd_varlen_fp16`` (packed variable-length batches), their sizing helpers,
 ``fa_status_string``, ``fa_get_device_status``, ``fa_num_sms``. ``attention``,
-``attention_decode`` and ``attention_backward`` are convenience wrappers that allocate outputs (and
+``attention_decode``, ``attention_varlen`` and ``attention_backward`` are convenience wrappers that allocate outputs (and
 the split-KV workspace) with torch and pick the entry point from the dtype.
 """
 from __future__ import annotations
@@ -35,6 +36,7 @@ FA_ERR_UNSUPPORTED = -4
 FA_ERR_LAUNCH = -5
 FA_ERR_TIMEOUT = -6
 FA_ERR_WORKSPACE = -7
+FA_ERR_SEQLENS = -8
 
 # Every symbol the header declares, with its ctypes signature.
 _vp = ctypes.c_void_p
@@ -57,6 +59,8 @@ SIGNATURES = {
                             [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_ulonglong, _vp]),
     "fa_fwd_splitkv_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp] + [ctypes.c_int] * 5 +
                                [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
+    "fa_fwd_varlen": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
+    "fa_fwd_varlen_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_bwd_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 4),
     "fa_bwd": (ctypes.c_int, [_vp] * 9 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp,
                                                                  ctypes.c_ulonglong, _vp]),
@@ -250,6 +254,50 @@ def attention_decode(q, k, v, scale=None, causal=False, n_splits=None, stream=No
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     fn = {torch.bfloat16: fa_fwd_splitkv, torch.float16: fa_fwd_splitkv_fp16}[q.dtype]
     fn(q, k, v, out, lse, scale, causal, n_splits, ws, stream)
+    return out, lse
+
+
+# ---------------------------------------------------------------- packed variable-length batch
+def _raw_varlen(fn_name, dtype, q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor [total, heads, d]")
+    total, H, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (total, Hkv, d) or v.shape != k.shape or out.shape != q.shape or H % Hkv:
+        raise ValueError("q, out: [total, H, d]; k, v: [total, Hkv, d] with Hkv dividing H")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (H, total):
+        raise ValueError("lse must be a contiguous CUDA float32 [H, total] tensor")
+    if (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or not cu_seqlens.is_contiguous()
+            or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2):
+        raise ValueError("cu_seqlens must be a contiguous CUDA int32 [nseq + 1] tensor")
+    nseq = cu_seqlens.numel() - 1
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens), nseq, total,
+                               int(max_seqlen), H, Hkv, d, float(scale), int(bool(causal)),
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_varlen(q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal, stream=None):
+    """bf16 forward over packed sequences: q, out [total, H, d], k, v [total, Hkv, d], lse [H, total]."""
+    _raw_varlen("fa_fwd_varlen", torch.bfloat16, q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal, stream)
+
+
+def fa_fwd_varlen_fp16(q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal, stream=None):
+    """fp16 forward over packed sequences."""
+    _raw_varlen("fa_fwd_varlen_fp16", torch.float16, q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal,
+                stream)
+
+
+def attention_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, stream=None):
+    """O [total, H, d] and lse [H, total] for packed sequences; allocates the outputs with torch."""
+    total, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    fn = {torch.bfloat16: fa_fwd_varlen, torch.float16: fa_fwd_varlen_fp16}[q.dtype]
+    fn(q, k, v, out, lse, cu_seqlens, max_seqlen, scale, causal, stream)
     return out, lse
 
 

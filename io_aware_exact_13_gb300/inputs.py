@@ -208,3 +208,69 @@ def make_bwd(B, H, N, d, dtype="bf16", seed=0):
     for _ in range(4):
         out.append(torch.randn((B, H, N, d), generator=g, dtype=torch.float32).to(t).contiguous())
     return tuple(out)
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+def varlen_lengths(total_tokens, lo, hi, seed):
+    """Sequence lengths for a packed batch: a CPU generator seeded with ``seed``
+    draws log-uniform lengths in [lo, hi] until their sum reaches total_tokens;
+    the last length is cut so that the lengths sum to exactly total_tokens."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out, acc = [], 0
+    while acc < total_tokens:
+        u = float(torch.rand((), generator=g))
+        L = int(round(math.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))))
+        L = min(L, total_tokens - acc)
+        out.append(L)
+        acc += L
+    return out
+
+
+def make_varlen(lengths, H, Hkv, d, dtype="bf16", seed=0):
+    """(q [total, H, d], k [total, Hkv, d], v [total, Hkv, d], cu_seqlens int32 [nseq + 1]) on the CPU:
+    fp32 standard normals drawn in the order q, k, v by a generator seeded with ``seed``, rounded to dtype."""
+    total = int(sum(lengths))
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    t = DTYPES[dtype]
+    q = torch.randn((total, H, d), generator=g, dtype=torch.float32).to(t).contiguous()
+    k = torch.randn((total, Hkv, d), generator=g, dtype=torch.float32).to(t).contiguous()
+    v = torch.randn((total, Hkv, d), generator=g, dtype=torch.float32).to(t).contiguous()
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return q, k, v, cu
+
+
+@dataclass(frozen=True)
+class VarlenWorkload:
+    total: int
+    lo: int
+    hi: int
+    H: int
+    d: int
+    dtype: str = "bf16"
+    causal: bool = True
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def lengths(self):
+        return varlen_lengths(self.total, self.lo, self.hi, self.seed)
+
+    def flops(self) -> float:
+        f = sum(4.0 * L * L * self.d * self.H for L in self.lengths())
+        return f / 2 if self.causal else f
+
+    def describe(self) -> dict:
+        L = self.lengths()
+        return {"total_tokens": self.total, "nseq": len(L), "len_min": min(L), "len_max": max(L),
+                "len_mix": f"log-uniform [{self.lo}, {self.hi}]", "H": self.H, "d": self.d, "dtype": self.dtype,
+                "causal": self.causal}
+
+
+VARLEN_WORKLOADS = {
+    "varlen_t65536_h32_d128_bf16_causal": VarlenWorkload(65536, 256, 8192, 32, 128, "bf16", True, seed=7100),
+}

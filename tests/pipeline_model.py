@@ -52,10 +52,13 @@ class Deadlock(AssertionError):
     pass
 
 
-def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, rescale_prob=0.1):
+def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, rescale_prob=0.1,
+             skip_empty_items=True):
     """Run one CTA's item list (first query rows) to completion; raise Deadlock or
     AssertionError on a protocol fault. ``per_buffer_p=False`` models a single
-    P-ready barrier per tile (a protocol that is known to alias)."""
+    P-ready barrier per tile (a protocol that is known to alias);
+    ``skip_empty_items=False`` a producer that loads K block 0 even for an item
+    with no rows (known to leave the K ring out of step)."""
     rnd = random.Random(seed)
     B = {}
 
@@ -82,7 +85,9 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
         return (f"p_full{t}{g & 1}", g >> 1) if per_buffer_p else (f"p_full{t}", g)
 
     def counts(q0):
-        n = [tile_nkv(N, causal, q0, t) for t in range(2)]
+        # an item is a first query row, or (first row, sequence length) in a packed batch
+        q0, n_seq = (q0, N) if isinstance(q0, int) else q0
+        n = [tile_nkv(n_seq, causal, q0, t) for t in range(2)]
         return n, max(n)
 
     def producer():
@@ -94,7 +99,8 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
                     yield ("wait", f"q_empty{t}", qcount[t] - 1)
                     tma.append(f"q_full{t}")
                     qcount[t] += 1
-            order = ["K"] + [x for j in range(nmax) for x in (["K"] if j + 1 < nmax else []) + ["V"]]
+            order = (["K"] if nmax > 0 or not skip_empty_items else []) + [x for j in range(nmax)
+                                                   for x in (["K"] if j + 1 < nmax else []) + ["V"]]
             for kind in order:
                 if kind == "K":
                     yield ("wait", f"k_empty{kpos % ring}", kpos // ring - 1)

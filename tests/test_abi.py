@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 
 def test_status_strings(fa):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(12345) == "unknown status"
@@ -166,3 +166,23 @@ def test_bwd_workspace_size(fa):
     assert fa.fa_bwd_workspace_bytes(1, 1, 1, 64) == 256 + 2 * 512
     with pytest.raises(fa.FAError):
         fa.fa_bwd_workspace_bytes(1, 1, 16, 80)
+
+
+@pytest.mark.parametrize("name", ["fa_fwd_varlen", "fa_fwd_varlen_fp16"])
+def test_varlen_host_validation(fa, name):
+    f = getattr(fa.lib, name)
+
+    def call(ptrs=(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000), nseq=2, total=100, maxlen=64, H=2, Hkv=2,
+             d=64):
+        return f(*[ctypes.c_void_p(x) if x else None for x in ptrs], nseq, total, maxlen, H, Hkv, d,
+                 ctypes.c_float(0.125), 1, None)
+
+    assert call(ptrs=(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0)) == fa.FA_ERR_NULL
+    assert call(ptrs=(0x10008, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000)) == fa.FA_ERR_ALIGN
+    assert call(ptrs=(0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60002)) == fa.FA_ERR_ALIGN
+    assert call(nseq=0) == fa.FA_ERR_SHAPE
+    assert call(total=0) == fa.FA_ERR_SHAPE
+    assert call(maxlen=0) == fa.FA_ERR_SHAPE
+    assert call(H=3, Hkv=2) == fa.FA_ERR_SHAPE
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_status_string(fa.FA_ERR_SEQLENS) != "unknown status"

@@ -44,3 +44,22 @@ def test_backward_protocol_completes_without_aliasing(n_it, stages):
 
     for seed in range(20):
         assert simulate_bwd(n_it, stages, seed)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("ring", [2, 5])
+def test_packed_batch_items_with_no_rows(causal, ring):
+    """Packed batches have items whose sequence is shorter than the item's
+    first row (nothing to do); the producer must not fill a K slot for them."""
+    lengths = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 0, 300]
+    n_items = (max(lengths) + ROWS - 1) // ROWS
+    items = [(qb * ROWS, L) for qb in range(n_items - 1, -1, -1) for L in lengths]
+    for seed in range(8):
+        assert simulate(max(lengths), causal, items, ring, seed)
+
+
+def test_loading_k_for_an_empty_item_is_caught():
+    lengths = [0, 1, 300, 0, 1000]
+    items = [(qb * ROWS, L) for qb in range(3, -1, -1) for L in lengths]
+    with pytest.raises(AssertionError):
+        simulate(1000, True, items, 2, 0, skip_empty_items=False)
