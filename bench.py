@@ -532,19 +532,21 @@ def run_bwd(args, w):
         bwd()
 
     peak_ours = peak_of(ours_fwd_bwd)
-    peak_mat = peak_of(mat_fwd_bwd)
-    p, bwd = materialised_backward(qd, kd, vd, dod, w.scale, w.causal)
-    for _ in range(3):
-        bwd()
-    torch.cuda.synchronize(dev)
-    m_steps = max(1, min(args.steps, 50))
-    a.record(stream)
-    for _ in range(m_steps):
-        bwd()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    mat_ms = a.elapsed_time(b) / m_steps
-    del p, bwd
+    peak_mat = mat_ms = None
+    if not args.no_materialised:
+        peak_mat = peak_of(mat_fwd_bwd)
+        p, bwd = materialised_backward(qd, kd, vd, dod, w.scale, w.causal)
+        for _ in range(3):
+            bwd()
+        torch.cuda.synchronize(dev)
+        m_steps = max(1, min(args.steps, 50))
+        a.record(stream)
+        for _ in range(m_steps):
+            bwd()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        mat_ms = a.elapsed_time(b) / m_steps
+        del p, bwd
     if rank != 0:
         return 0
     peak, src = load_peak()
@@ -579,6 +581,8 @@ def main():
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-materialised", action="store_true",
+                    help="backward workloads: skip the materialised comparison leg")
     args = ap.parse_args()
     if args.workload in DECODE_WORKLOADS:
         return run_decode(args, DECODE_WORKLOADS[args.workload])
