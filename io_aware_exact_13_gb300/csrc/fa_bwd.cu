@@ -114,6 +114,63 @@ __device__ __forceinline__ uint32_t pk2(float lo, float hi) {
     }
 }
 
+// P and dS for 32 query columns of one key (this thread's TMEM lane), packed in
+// pairs to the 16-bit input type: P = 2^(S * scale * log2 e - lse * log2 e) and
+// dS = P (dP - D). neg_l and neg_d are shared-memory addresses of -lse*log2e and
+// -D for the 32 columns (the same for every lane: broadcast loads). Keys past
+// the end, and (causal) keys after the query, get P = dS = 0.
+template <typename T, bool CAUSAL>
+__device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[32], const uint32_t (&dpv)[32], uint32_t neg_l,
+                                           uint32_t neg_d, float scale_log2, bool need_mask, bool key_ok, int key,
+                                           int q_first, uint32_t (&pp)[16], uint32_t (&dsp)[16]) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 4) {
+        const float4 nl = ld_shared_v4f(neg_l + c * 4);
+        const float4 nd = ld_shared_v4f(neg_d + c * 4);
+#pragma unroll
+        for (int h = 0; h < 4; h += 2) {
+            const float2 x = ffma2(make_float2(__uint_as_float(sv[c + h]), __uint_as_float(sv[c + h + 1])),
+                                   make_float2(scale_log2, scale_log2),
+                                   h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
+            float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (need_mask) {
+                const int q0 = q_first + c + h;
+                const bool v0 = key_ok && (!CAUSAL || key <= q0);
+                const bool v1 = key_ok && (!CAUSAL || key <= q0 + 1);
+                pe.x = v0 ? pe.x : 0.0f;
+                pe.y = v1 ? pe.y : 0.0f;
+            }
+            const float2 t = fadd2(make_float2(__uint_as_float(dpv[c + h]), __uint_as_float(dpv[c + h + 1])),
+                                   h == 0 ? make_float2(nd.x, nd.y) : make_float2(nd.z, nd.w));
+            const float2 ds = fmul2(pe, t);
+            pp[(c + h) / 2] = pk2<T>(pe.x, pe.y);
+            dsp[(c + h) / 2] = pk2<T>(ds.x, ds.y);
+        }
+    }
+}
+
+// Stage one 32 x 32 fp32 tile (this warp's 32 rows x 32 head columns, already
+// scaled) in shared memory with the 128-byte swizzle of tm_dq, and reduce-add it
+// into the dQ accumulator. Lane 0 first waits until its previous reduction from
+// the same staging area has been read.
+__device__ __forceinline__ void stage_and_reduce_dq(const CUtensorMap *tm_dq, uint32_t box, const uint32_t (&qv)[32],
+                                                    float mul, int lane, int x, int y, int z) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        st_shared_v4(box + lane * 128 + ((u ^ (lane & 7)) * 16), __float_as_uint(__uint_as_float(qv[4 * u]) * mul),
+                     __float_as_uint(__uint_as_float(qv[4 * u + 1]) * mul),
+                     __float_as_uint(__uint_as_float(qv[4 * u + 2]) * mul),
+                     __float_as_uint(__uint_as_float(qv[4 * u + 3]) * mul));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_reduce_add_3d(tm_dq, box, x, y, z);
+        bulk_commit_group();
+    }
+}
+
 template <typename T, int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -284,30 +341,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_wait(tmem + lane_base + c0, sv, tmem + lane_base + 128 + c0, dpv);
                 uint32_t pp[16], dsp[16];
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 nl = ld_shared_v4f(stats + (c0 + c) * 4);        // -lse2, same for the warp
-                    const float4 nd = ld_shared_v4f(stats + (128 + c0 + c) * 4);  // -D
-#pragma unroll
-                    for (int h = 0; h < 4; h += 2) {
-                        const float2 x = ffma2(make_float2(__uint_as_float(sv[c + h]), __uint_as_float(sv[c + h + 1])),
-                                               make_float2(p.scale_log2, p.scale_log2),
-                                               h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
-                        float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        if (need_mask) {
-                            const int q0 = row0 + c0 + c + h;
-                            const bool v0 = key_ok && (!CAUSAL || key <= q0);
-                            const bool v1 = key_ok && (!CAUSAL || key <= q0 + 1);
-                            pe.x = v0 ? pe.x : 0.0f;
-                            pe.y = v1 ? pe.y : 0.0f;
-                        }
-                        const float2 t = fadd2(make_float2(__uint_as_float(dpv[c + h]), __uint_as_float(dpv[c + h + 1])),
-                                               h == 0 ? make_float2(nd.x, nd.y) : make_float2(nd.z, nd.w));
-                        const float2 ds = fmul2(pe, t);
-                        pp[(c + h) / 2] = pk2<T>(pe.x, pe.y);
-                        dsp[(c + h) / 2] = pk2<T>(ds.x, ds.y);
-                    }
-                }
+                p_ds_chunk<T, CAUSAL>(sv, dpv, stats + c0 * 4, stats + (128 + c0) * 4, p.scale_log2, need_mask, key_ok,
+                                      key, row0 + c0, pp, dsp);
                 // P^T and dS^T overwrite columns this warpgroup has already read.
                 tmem_st16(tmem + lane_base + 0 + pcol, pp);
                 tmem_st16(tmem + lane_base + 128 + pcol, dsp);
@@ -404,6 +439,293 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// d = 64: the same products with the tensor core and the gradient warps
+// overlapped. Each 128-row query block is handled as two 64-row halves h (A =
+// rows 0-63, B = rows 64-127), gradient warpgroup h owning half h, with their
+// own barriers. The tensor core runs, per block i,
+//   dV,dK(A, i)   S,dP(A, i+1)   dV,dK(B, i)   dQ(i)   S,dP(B, i+1)
+// so that each warpgroup's P/dS pass of one block overlaps the other half's
+// products (the two warpgroups alternate like a ping-pong). dS is kept in two
+// shared-memory buffers (block parity), because the pass of half A of block
+// i+1 runs before dQ(i) has read dS(i). dQ of block i is read out by the
+// gradient warps after their pass of block i+1 (it has its own tensor-memory
+// columns and its own staging buffer); dQ(i+1) waits for that read-out.
+// Tensor memory: S_A [0,64), dP_A [64,128), S_B [128,192), dP_B [192,256),
+// dV [256,320), dK [320,384), dQ [384,448). Each half's P^T and dS^T are packed
+// into the first 32 columns of its own S and dP ranges (columns its warpgroup
+// has already read).
+template <typename T>
+struct BwdCfgH64 {
+    static constexpr int D = 64;
+    static constexpr int CHUNK = 128 * 128;          // 128 rows x 128 bytes (one tile at d = 64)
+    static constexpr int STAGES = 2;
+    static constexpr int SMEM_K = 0;
+    static constexpr int SMEM_V = CHUNK;
+    static constexpr int SMEM_QD = 2 * CHUNK;                      // STAGES x (Q_i, dO_i)
+    static constexpr int SMEM_DS = SMEM_QD + STAGES * 2 * CHUNK;   // dS[2]: queries 0-63 | 64-127, 128 keys each
+    static constexpr int SMEM_STAGE = SMEM_DS + 4 * CHUNK;         // dQ staging: 8 boxes of 32 x 32 fp32
+    static constexpr int SMEM_STATS = SMEM_STAGE + 8 * 4096;       // [half][buffer][-lse2 x64, -D x64]
+    static constexpr int SMEM_BAR = SMEM_STATS + 2 * 2 * 128 * 4;
+    // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], acc[2], dq_full, dq_free, stats[2], drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
+    static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;
+    static constexpr uint32_t FMT = Elem<T>::fmt;
+    static constexpr uint32_t ID_S = make_idesc_ab(FMT, 128, 64, 0, 0);   // S_h^T, dP_h^T: 128 keys x 64 queries
+    static constexpr uint32_t ID_ACC = make_idesc_ab(FMT, 128, 64, 0, 1); // dV, dK: A in TMEM, B N-major
+    static constexpr uint32_t ID_DQ = make_idesc_ab(FMT, 128, 64, 1, 1);  // dQ: A M-major, B N-major
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+template <typename T, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel_h64(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+    using C = BwdCfgH64<T>;
+    constexpr int ST = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR);
+    const uint32_t bar_kv = smem_u32(bars);
+    auto bar_qd_full = [&](int s) { return smem_u32(bars + 1 + s); };
+    auto bar_qd_empty = [&](int s) { return smem_u32(bars + 1 + ST + s); };
+    auto bar_sp_full = [&](int h) { return smem_u32(bars + 1 + 2 * ST + h); };  // S_h, dP_h computed
+    auto bar_p_full = [&](int h) { return smem_u32(bars + 3 + 2 * ST + h); };   // half h packed (128 arrivals)
+    auto bar_acc = [&](int h) { return smem_u32(bars + 5 + 2 * ST + h); };      // dV, dK of half h done
+    const uint32_t bar_dq_full = smem_u32(bars + 7 + 2 * ST);                  // dQ of the block computed
+    const uint32_t bar_dq_free = smem_u32(bars + 8 + 2 * ST);                  // dQ loaded by all (256 arrivals)
+    auto bar_stats = [&](int h) { return smem_u32(bars + 9 + 2 * ST + h); };   // half h statistics (128 arrivals)
+    const uint32_t bar_drain = smem_u32(bars + 11 + 2 * ST);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x % p.BH;
+    const int j = blockIdx.x / p.BH;
+    const int n_qblk = p.Npad / kBlk;
+    const int i0 = CAUSAL ? j : 0;
+    const int n_it = n_qblk - i0;  // >= 1
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(bar_qd_full(s), 1);
+            mbar_init(bar_qd_empty(s), 1);
+        }
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar_sp_full(h), 1);
+            mbar_init(bar_p_full(h), 128);
+            mbar_init(bar_acc(h), 1);
+            mbar_init(bar_stats(h), 128);
+        }
+        mbar_init(bar_dq_full, 1);
+        mbar_init(bar_dq_free, kGradThreads);
+        mbar_init(bar_drain, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_last();
+            mbar_arrive_expect_tx(bar_kv, 2 * C::CHUNK);
+            tma_load_3d(smem_u32(smem + C::SMEM_K), &tm_k, bar_kv, 0, j * kBlk, bh, pol);
+            tma_load_3d(smem_u32(smem + C::SMEM_V), &tm_v, bar_kv, 0, j * kBlk, bh, pol);
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int s = it % ST;
+                if (!bwd_wait(bar_qd_empty(s), ((it / ST) & 1u) ^ 1u, p)) break;
+                const uint32_t dst = smem_u32(smem + C::SMEM_QD + s * 2 * C::CHUNK);
+                mbar_arrive_expect_tx(bar_qd_full(s), 2 * C::CHUNK);
+                const int row0 = (i0 + it) * kBlk;
+                tma_load_3d(dst, &tm_q, bar_qd_full(s), 0, row0, bh, pol);
+                tma_load_3d(dst + C::CHUNK, &tm_do, bar_qd_full(s), 0, row0, bh, pol);
+                issued = it + 1;
+            }
+            bwd_wait(bar_kv, 0, p);  // every copy into this CTA's shared memory lands before exit
+            for (int it = issued - ST > 0 ? issued - ST : 0; it < issued; ++it)
+                bwd_wait(bar_qd_full(it % ST), (it / ST) & 1u, p);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        const uint32_t issue = lane == 0 ? 1u : 0u;
+        const uint64_t k_km = smem_desc_sw128(smem_u32(smem + C::SMEM_K), 16, 1024);
+        const uint64_t v_km = smem_desc_sw128(smem_u32(smem + C::SMEM_V), 16, 1024);
+        const uint64_t k_mn = smem_desc_sw128(smem_u32(smem + C::SMEM_K), C::CHUNK, 1024);
+        // S_h^T = K_j Q_h^T, dP_h^T = V_j dO_h^T of block it (query rows 64h.. of the stage = +8 KB)
+        auto issue_s = [&](int it, int h) {
+            const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
+            const uint64_t q_km = smem_desc_sw128(q_s, 16, 1024);
+            const uint64_t do_km = smem_desc_sw128(q_s + C::CHUNK, 16, 1024);
+            const uint64_t hoff = (uint64_t)((h * 64 * 128) >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t off = (uint64_t)((k * 32) >> 4);
+                mma_ss(tmem + 128 * h, k_km + off, q_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
+                mma_ss(tmem + 128 * h + 64, v_km + off, do_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
+            }
+            tc_commit(bar_sp_full(h), issue);
+        };
+        // dV_j += P_h^T dO_h, dK_j += dS_h^T Q_h, contracted over the 64 rows of half h of block it
+        auto issue_acc = [&](int it, int h) {
+            const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
+            const uint64_t q_mn = smem_desc_sw128(q_s, C::CHUNK, 1024);
+            const uint64_t do_mn = smem_desc_sw128(q_s + C::CHUNK, C::CHUNK, 1024);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t off = (uint64_t)(((h * 64 + k * 16) * 128) >> 4);
+                const uint32_t acc = (it > 0 || h > 0 || k > 0) ? 1u : 0u;
+                mma_ts(tmem + 256, tmem + 128 * h + 8 * k, do_mn + off, C::ID_ACC, acc, issue);
+                mma_ts(tmem + 320, tmem + 128 * h + 64 + 8 * k, q_mn + off, C::ID_ACC, acc, issue);
+            }
+            tc_commit(bar_acc(h), issue);
+        };
+        bool ok = bwd_wait_warp(bar_kv, 0, p) && bwd_wait_warp(bar_qd_full(0), 0, p);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, 0);
+            issue_s(0, 1);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+            const bool next = it + 1 < n_it;
+            ok = bwd_wait_warp(bar_p_full(0), it & 1u, p);
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(it, 0);
+            if (next) {  // S_A of the next block once dV, dK(A) have read half A's columns
+                ok = bwd_wait_warp(bar_qd_full((it + 1) % ST), ((it + 1) / ST) & 1u, p) &&
+                     bwd_wait_warp(bar_acc(0), it & 1u, p);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(it + 1, 0);
+            }
+            ok = bwd_wait_warp(bar_p_full(1), it & 1u, p);
+            if (!ok) break;
+            tc_fence_after();
+            issue_acc(it, 1);
+            tc_commit(bar_qd_empty(it % ST), issue);  // every reader of this Q, dO stage is issued
+            if (it > 0) ok = bwd_wait_warp(bar_dq_free, (it - 1) & 1u, p);  // dQ of the last block read out
+            if (!ok) break;
+            tc_fence_after();
+            // dQ_i = dS_i K_j, contracted over the 128 keys (dS buffer it & 1)
+            const uint64_t ds_mn =
+                smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK), C::CHUNK, 1024);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                mma_ss(tmem + 384, ds_mn + off, k_mn + off, C::ID_DQ, k > 0 ? 1u : 0u, issue);
+            }
+            tc_commit(bar_dq_full, issue);
+            if (next) {  // S_B of the next block once dV, dK(B) have read half B's columns
+                ok = bwd_wait_warp(bar_acc(1), it & 1u, p);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(it + 1, 1);
+            }
+        }
+        tc_commit(bar_drain, issue);
+        bwd_wait_warp(bar_drain, 0, p);
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- gradient warps
+        const int g = (warp - 4) >> 2;  // half of the query block
+        const int w = warp & 3;
+        const int r = w * 32 + lane;    // TMEM lane: key r, later query row r
+        const uint32_t lane_base = (uint32_t)(w * 32) << 16;
+        const uint32_t s_col = tmem + lane_base + 128u * g;  // S_g; dP_g at +64
+        const int key = j * kBlk + r;
+        const bool key_ok = key < p.N;
+        const bool ragged_keys = (j + 1) * kBlk > p.N;
+        const uint32_t ds_row0 = smem_u32(smem + C::SMEM_DS) + g * C::CHUNK + r * 128;  // + (block & 1) * 32 KB
+        const uint32_t box = smem_u32(smem + C::SMEM_STAGE) + (g * 4 + w) * 4096;
+        const uint32_t stats0 = smem_u32(smem + C::SMEM_STATS) + g * 1024;  // + buffer * 512
+        // thread r hands over -lse2 (r < 64) or -D (r >= 64) of query row 64g + (r & 63)
+        const float *stat_src = (r < 64 ? p.lse2 : p.dsum) + (size_t)bh * p.Npad + 64 * g + (r & 63);
+        float stat_next = -__ldg(stat_src + i0 * kBlk);
+        bool ok = true;
+        auto readout = [&](int blk) -> bool {  // dQ rows of query block blk, head columns 32g..32g+31
+            if (!bwd_wait_warp(bar_dq_full, (uint32_t)(blk - i0) & 1u, p)) return false;
+            tc_fence_after();
+            uint32_t qv[32];
+            tmem_ld32_wait(tmem + lane_base + 384 + 32 * g, qv);
+            tc_fence_before();
+            mbar_arrive(bar_dq_free);
+            stage_and_reduce_dq(&tm_dq, box, qv, p.scale, lane, 32 * g, blk * kBlk + w * 32, bh);
+            return true;
+        };
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int i = i0 + it;
+            const uint32_t stats = stats0 + (it & 1) * 512;
+            st_shared_f32(stats + r * 4, stat_next);
+            mbar_arrive(bar_stats(g));
+            ok = bwd_wait_warp(bar_stats(g), it & 1u, p) && bwd_wait_warp(bar_sp_full(g), it & 1u, p);
+            if (!ok) break;
+            tc_fence_after();
+            const bool need_mask = ragged_keys || (CAUSAL && i == j);
+            const uint32_t ds_row = ds_row0 + (it & 1) * 2 * C::CHUNK;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t sv[32], dpv[32];
+                tmem_ld32x2_wait(s_col + c0, sv, s_col + 64 + c0, dpv);
+                uint32_t pp[16], dsp[16];
+                p_ds_chunk<T, CAUSAL>(sv, dpv, stats + c0 * 4, stats + (64 + c0) * 4, p.scale_log2, need_mask,
+                                      key_ok, key, i * kBlk + 64 * g + c0, pp, dsp);
+                tmem_st16(s_col + c0 / 2, pp);
+                tmem_st16(s_col + 64 + c0 / 2, dsp);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t unit = (uint32_t)((c0 / 8 + u) ^ (r & 7));
+                    st_shared_v4(ds_row + unit * 16, dsp[4 * u], dsp[4 * u + 1], dsp[4 * u + 2], dsp[4 * u + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar_p_full(g));
+            if (it + 1 < n_it) stat_next = -__ldg(stat_src + (i + 1) * kBlk);
+            if (it > 0) ok = readout(i - 1);
+        }
+        if (ok) ok = readout(i0 + n_it - 1);
+        if (lane == 0) bulk_wait_all();
+        // ---------------------------------------------------------------- dV_j (half A's group), dK_j (B's)
+        if (ok) {  // the last dq_full covers every dV and dK product
+            tc_fence_after();
+            const float mul = g == 0 ? 1.0f : p.scale;
+            T *dst = reinterpret_cast<T *>(g == 0 ? p.dv : p.dk) + ((size_t)bh * p.N + (size_t)(key_ok ? key : 0)) * 64;
+            uint32_t a[32], b[32];
+            tmem_ld32x2_wait(tmem + lane_base + 256 + 64 * g, a, tmem + lane_base + 256 + 64 * g + 32, b);
+            if (key_ok) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    st_global_v4(dst + c, pk2<T>(__uint_as_float(a[c]) * mul, __uint_as_float(a[c + 1]) * mul),
+                                 pk2<T>(__uint_as_float(a[c + 2]) * mul, __uint_as_float(a[c + 3]) * mul),
+                                 pk2<T>(__uint_as_float(a[c + 4]) * mul, __uint_as_float(a[c + 5]) * mul),
+                                 pk2<T>(__uint_as_float(a[c + 6]) * mul, __uint_as_float(a[c + 7]) * mul));
+                    st_global_v4(dst + 32 + c, pk2<T>(__uint_as_float(b[c]) * mul, __uint_as_float(b[c + 1]) * mul),
+                                 pk2<T>(__uint_as_float(b[c + 2]) * mul, __uint_as_float(b[c + 3]) * mul),
+                                 pk2<T>(__uint_as_float(b[c + 4]) * mul, __uint_as_float(b[c + 5]) * mul),
+                                 pk2<T>(__uint_as_float(b[c + 6]) * mul, __uint_as_float(b[c + 7]) * mul));
+                }
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // Row statistics for the backward, one warp per padded row:
 //   dsum = sum_t dO_t O_t (0 past N), lse2 = lse * log2(e) (+inf past N),
 // and the row's dQ accumulator is zeroed.
@@ -460,9 +782,10 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float *__restrict__ dq_
 
 template <typename T, int D, bool CAUSAL>
 int launch_bwd_variant(const BwdArgs &a) {
-    using C = BwdCfg<T, D>;
-    auto kern = fa_bwd_kernel<T, D, CAUSAL>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    // d = 64 runs the overlapped half-block kernel; d = 128 (tensor memory full) the serial one
+    auto kern = D == 64 ? fa_bwd_kernel_h64<T, CAUSAL> : fa_bwd_kernel<T, D, CAUSAL>;
+    const int smem_bytes = D == 64 ? BwdCfgH64<T>::SMEM_BYTES : BwdCfg<T, D>::SMEM_BYTES;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return -5;
     const int BH = a.B * a.H;
     const int Npad = static_cast<int>(bwd_padded_rows(a.N));
@@ -492,7 +815,7 @@ int launch_bwd_variant(const BwdArgs &a) {
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
     const int64_t grid = static_cast<int64_t>(BH) * (Npad / kBlk);
-    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<static_cast<unsigned>(grid), kBwdThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo, tdq, p);
     if (cudaGetLastError() != cudaSuccess) return -5;
     const size_t n4 = static_cast<size_t>(BH) * a.N * D / 4;
     fa_bwd_post<T><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dq_acc, static_cast<T *>(a.dq),

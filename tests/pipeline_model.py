@@ -275,3 +275,99 @@ def simulate_bwd(n_it, stages, seed, grad_warps=8):
             del agents[c]
             waiting[c] = None
     return True
+
+
+def simulate_bwd_halves(n_it, stages, seed):
+    """Protocol of the d = 64 backward kernel that overlaps the two 64-row halves
+    of each query block: S/dP per half, dV/dK per half, the next block's S/dP
+    issued between them, dQ of block i read out by the gradient warpgroups
+    after their pass of block i + 1."""
+    rnd = random.Random(seed)
+    B = {}
+    for name, c in (("kv", 1), ("dq_full", 1), ("dq_free", 256), ("drain", 1)):
+        B[name] = Bar(name, c)
+    for h in range(2):
+        for name, c in (("sp_full", 1), ("p_full", 128), ("acc", 1), ("stats", 128)):
+            B[f"{name}{h}"] = Bar(f"{name}{h}", c)
+    for s in range(stages):
+        B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
+        B[f"qd_empty{s}"] = Bar(f"qd_empty{s}", 1)
+    tensor_pipe, tma = [], []
+
+    def producer():
+        tma.append("kv")
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_empty{s}", it // stages - 1)
+            tma.append(f"qd_full{s}")
+
+    def mma():
+        # per block: dV,dK(A, i)  S,dP(A, i+1)  dV,dK(B, i)  dQ(i)  S,dP(B, i+1)
+        yield ("wait", "kv", 0)
+        yield ("wait", "qd_full0", 0)
+        tensor_pipe.extend([("commit", "sp_full0"), ("commit", "sp_full1")])
+        for it in range(n_it):
+            nxt = it + 1 < n_it
+            yield ("wait", "p_full0", it)
+            tensor_pipe.append(("commit", "acc0"))
+            if nxt:
+                s1 = (it + 1) % stages
+                yield ("wait", f"qd_full{s1}", (it + 1) // stages)
+                yield ("wait", "acc0", it)
+                tensor_pipe.append(("commit", "sp_full0"))
+            yield ("wait", "p_full1", it)
+            tensor_pipe.extend([("commit", "acc1"), ("commit", f"qd_empty{it % stages}")])
+            if it > 0:
+                yield ("wait", "dq_free", it - 1)
+            tensor_pipe.append(("commit", "dq_full"))
+            if nxt:
+                yield ("wait", "acc1", it)
+                tensor_pipe.append(("commit", "sp_full1"))
+        tensor_pipe.append(("commit", "drain"))
+        yield ("wait", "drain", 0)
+
+    def grads(h):
+        def readout(blk):
+            yield ("wait", "dq_full", blk)
+            yield ("arrive", "dq_free", 32)
+        for it in range(n_it):
+            yield ("arrive", f"stats{h}", 32)
+            yield ("wait", f"stats{h}", it)
+            yield ("wait", f"sp_full{h}", it)
+            yield ("arrive", f"p_full{h}", 32)
+            if it > 0:
+                yield from readout(it - 1)
+        yield from readout(n_it - 1)
+
+    agents = {"producer": producer(), "mma": mma()}
+    for h in range(2):
+        for w in range(4):
+            agents[f"g{h}.{w}"] = grads(h)
+    waiting = {k: None for k in agents}
+    while agents or tensor_pipe or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        if tensor_pipe:
+            ready.append("#tensor")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c == "#tensor":
+            B[tensor_pipe.pop(0)[1]].arrive(1)
+            continue
+        if c == "#tma":
+            B[tma.pop(rnd.randrange(len(tma)))].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

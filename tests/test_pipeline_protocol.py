@@ -63,3 +63,11 @@ def test_loading_k_for_an_empty_item_is_caught():
     items = [(qb * ROWS, L) for qb in range(3, -1, -1) for L in lengths]
     with pytest.raises(AssertionError):
         simulate(1000, True, items, 2, 0, skip_empty_items=False)
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 32])
+def test_backward_half_block_protocol(n_it):
+    from pipeline_model import simulate_bwd_halves
+
+    for seed in range(20):
+        assert simulate_bwd_halves(n_it, 2, seed)
