@@ -175,6 +175,12 @@ def max_over_ranks(world, x: float, dev) -> float:
     return float(t.item())
 
 
+def whole_job_rate(world: int, units_per_rank: float, max_ms: float) -> float:
+    """Units per second of the whole job: every rank processes its own copy of the
+    workload, and the slowest rank's time (max over ranks) is the job's time."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
 def oracle_sample(w, q, k, v, mask, n_rows: int, seed: int):
     """Time the fp64 oracle on n_rows sampled query rows; return (seconds, flops, threads)."""
     import oracle
@@ -278,7 +284,7 @@ def run_ours(args, w):
     if status != 0:
         raise SystemExit(f"device status word {status} after the timed region")
     ms_per_step = total_ms / args.steps
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(world, w.flops * args.steps, total_ms) / 1e12
 
     # ---------------------------------------------------------------- end to end through host buffers
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()

@@ -188,6 +188,15 @@ const char *fa_status_string(int status);
  * synchronisation itself fails. */
 int fa_get_device_status(void *stream);
 
+/* Failure-detection self-test (the pages have no counterpart; it checks this
+ * library's own error path). Enqueues one warp that waits on an mbarrier that
+ * nothing ever completes, through the same bounded wait that every pipeline
+ * role of every kernel uses. After timeout_ns (1 ns .. 1 s) the wait gives up,
+ * FA_ERR_TIMEOUT is recorded in the device status word and the kernel exits;
+ * the CUDA context stays usable. Returns FA_OK once enqueued, FA_ERR_SHAPE for
+ * a timeout outside that range. */
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void *stream);
+
 /* Number of streaming multiprocessors the persistent grid is sized for on the
  * current device, or a negative status. */
 int fa_num_sms(void);

@@ -266,6 +266,22 @@ bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes
     return r == CUDA_SUCCESS;
 }
 
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing
+// ever completes, through the same wait routine every pipeline role uses. The
+// wait gives up after p.timeout_ns, records FA_ERR_TIMEOUT in the device status
+// word and returns; the kernel then exits normally.
+__global__ void fa_selftest_wait_kernel(FwdParams p) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    wait_warp(smem_u32(&bar), 0, &abort_flag, p);
+}
+
 bool encode_tokens_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d,
                        int heads, int total, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
@@ -378,6 +394,17 @@ int fa_bwd_fp16(const void *q, const void *k, const void *v, const void *out, co
                 unsigned long long workspace_bytes, void *stream) {
     return bwd_common(true, q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                       workspace_bytes, stream);
+}
+
+int fa_selftest_wait_timeout(unsigned long long timeout_ns, void *stream) {
+    if (timeout_ns == 0 || timeout_ns > 1000000000ull) return FA_ERR_SHAPE;
+    DeviceInfo *di = device_info();
+    if (!di) return FA_ERR_LAUNCH;
+    fa::FwdParams p = {};
+    p.status = di->status;
+    p.timeout_ns = timeout_ns;
+    fa::fa_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 const char *fa_status_string(int status) {

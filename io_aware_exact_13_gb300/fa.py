@@ -61,6 +61,7 @@ SIGNATURES = {
                                [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
     "fa_fwd_varlen": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_varlen_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
+    "fa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_ulonglong, _vp]),
     "fa_bwd_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 4),
     "fa_bwd": (ctypes.c_int, [_vp] * 9 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp,
                                                                  ctypes.c_ulonglong, _vp]),
@@ -354,6 +355,14 @@ def attention_backward(q, k, v, out, dout, lse, scale=None, causal=False, worksp
 
 def fa_get_device_status(stream=None) -> int:
     return int(lib.fa_get_device_status(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def fa_selftest_wait_timeout(timeout_ns, stream=None):
+    """Enqueue the bounded-wait self-test (a wait nothing completes); afterwards
+    fa_get_device_status() must report FA_ERR_TIMEOUT."""
+    rc = lib.fa_selftest_wait_timeout(int(timeout_ns), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_selftest_wait_timeout")
 
 
 def fa_num_sms() -> int:
