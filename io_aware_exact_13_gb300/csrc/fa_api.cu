@@ -317,13 +317,15 @@ int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_o
 }
 
 int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d) {
-    (void)Nq;
-    (void)d;
-    if (B < 1 || H < 1 || Nk < 1) return FA_ERR_SHAPE;
+    if (B < 1 || H < 1 || Nk < 1 || Nq < 1) return FA_ERR_SHAPE;
     DeviceInfo *di = device_info();
     const int64_t sms = di ? di->num_sms : 148;
     const int64_t bh = static_cast<int64_t>(B) * H;
-    int64_t n = (4 * sms + bh - 1) / bh;  // about four CTAs per SM
+    // Fill the GPU in exactly one wave: as many splits per head as there are
+    // resident CTA slots per head (a partly filled second wave would cost
+    // almost a whole extra wave of time).
+    const int64_t slots = sms * fa::splitkv_blocks_per_sm(d == 64 ? 64 : 128, Nq);
+    int64_t n = slots / bh;
     const int64_t max_by_len = (static_cast<int64_t>(Nk) + 63) / 64;  // at least ~64 keys per split
     if (n > max_by_len) n = max_by_len;
     if (n > 1024) n = 1024;

@@ -174,6 +174,169 @@ __global__ void __launch_bounds__(kWarpsSK * 32) fa_splitkv_partial(const T *__r
     }
 }
 
+// Several query rows per head (2 <= Nq <= 16). With one key row per warp every
+// key costs log2(32) shuffle steps per query row, which makes the kernel
+// issue-bound long before HBM is busy. Here a group of L lanes owns one key row
+// (each lane D/L consecutive elements), so a warp handles 32/L keys per step and
+// a dot product needs only log2(L) shuffle steps. Each lane group keeps its own
+// running (m, l, acc) per query row, with the lazy rescaling of the forward
+// (the reference maximum moves only when a score exceeds it by more than
+// kTauSK, in log2 units); the groups and then the warps are merged with the
+// same block-summary rule as the combine kernel.
+constexpr float kTauSK = 8.0f;
+
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T *src, float (&f)[E]) {
+    // E consecutive 16-bit elements, E in {4, 8, 16}: 8- or 16-byte loads
+    if constexpr (E == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(src));
+        const T *h = reinterpret_cast<const T *>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] = Vec<T>::to_f(h[e]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < E / 8; ++c) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+            const T *h = reinterpret_cast<const T *>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[8 * c + e] = Vec<T>::to_f(h[e]);
+        }
+    }
+}
+
+template <typename T, int D, int NQ, int L, bool CAUSAL>
+__global__ void __launch_bounds__(kWarpsSK * 32) fa_splitkv_partial_lg(
+    const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ o_part,
+    float *__restrict__ lse_part, int BH, int Nq, int Nk, int split_len, float scale_log2) {
+    constexpr int G = 32 / L;  // key rows per warp step
+    constexpr int E = D / L;   // elements of a row per lane
+    constexpr int STEP = kWarpsSK * G;
+    const int split = blockIdx.x, bh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = lane / L, li = lane % L;
+    const int k0 = split * split_len, k1 = min(Nk, k0 + split_len);
+    const T *qb = q + (size_t)bh * Nq * D + li * E;
+    const T *kb = k + (size_t)bh * Nk * D + li * E;
+    const T *vb = v + (size_t)bh * Nk * D + li * E;
+
+    float qf[NQ][E], acc[NQ][E], m[NQ], l[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
+        if (i < Nq) {
+            load_vec<T, E>(qb + (size_t)i * D, qf[i]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) qf[i][e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+    }
+    const int shift = Nk - Nq;  // causal: query i sees keys j <= i + shift
+    for (int j0 = k0 + warp * G + gi; j0 < k1 + gi; j0 += 2 * STEP) {
+        float kf[2][E], vf[2][E];
+        bool ok[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {  // two key rows in flight per lane
+            const int j = j0 + u * STEP;
+            ok[u] = j < k1;
+            if (ok[u]) {
+                load_vec<T, E>(kb + (size_t)j * D, kf[u]);
+                load_vec<T, E>(vb + (size_t)j * D, vf[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) kf[u][e] = vf[u][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            if (i >= Nq) break;
+            float sc[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float part = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) part = fmaf(qf[i][e], kf[u][e], part);
+                sc[u] = part;
+            }
+#pragma unroll
+            for (int off = L / 2; off > 0; off >>= 1)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], off);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = j0 + u * STEP;
+                const bool vis = ok[u] && (!CAUSAL || j <= i + shift);
+                const float x = vis ? sc[u] * scale_log2 : -INFINITY;
+                if (x > m[i] + kTauSK) {  // (also true for the first visible key, m = -inf)
+                    const float corr = ex2_approx(m[i] - x);  // 0 when m was -inf
+                    l[i] *= corr;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[i][e] *= corr;
+                    m[i] = x;
+                }
+                const float pu = vis ? ex2_approx(x - m[i]) : 0.f;
+                l[i] += pu;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[i][e] = fmaf(pu, vf[u][e], acc[i][e]);
+            }
+        }
+    }
+    // merge the G lane groups of the warp (lanes li, li + L, li + 2L, ... hold the same elements)
+#pragma unroll
+    for (int off = L; off < 32; off <<= 1) {
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m[i], off);
+            const float lo = __shfl_xor_sync(0xffffffffu, l[i], off);
+            const float mn = fmaxf(m[i], mo);
+            const float fa = mn == -INFINITY ? 0.f : ex2_approx(m[i] - mn);
+            const float fb = mn == -INFINITY ? 0.f : ex2_approx(mo - mn);
+            l[i] = l[i] * fa + lo * fb;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float ao = __shfl_xor_sync(0xffffffffu, acc[i][e], off);
+                acc[i][e] = acc[i][e] * fa + ao * fb;
+            }
+            m[i] = mn;
+        }
+    }
+    // merge the four warps' summaries of this split
+    __shared__ float sm_m[kWarpsSK][NQ], sm_l[kWarpsSK][NQ];
+    __shared__ float sm_a[kWarpsSK][NQ][D];
+    if (gi == 0) {
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            if (li == 0) {
+                sm_m[warp][i] = m[i];
+                sm_l[warp][i] = l[i];
+            }
+#pragma unroll
+            for (int e = 0; e < E; ++e) sm_a[warp][i][li * E + e] = acc[i][e];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < Nq * D; idx += kWarpsSK * 32) {
+        const int i = idx / D, e = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarpsSK; ++w) M = fmaxf(M, sm_m[w][i]);
+        float Lsum = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarpsSK; ++w) {
+                const float f = ex2_approx(sm_m[w][i] - M);  // 0 for an empty warp
+                Lsum += f * sm_l[w][i];
+                A += f * sm_a[w][i][e];
+            }
+        }
+        const size_t row = ((size_t)split * BH + bh) * Nq + i;
+        o_part[row * D + e] = Lsum > 0.f ? A / Lsum : 0.f;
+        if (e == 0) lse_part[row] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * 0.6931471805599453f : -INFINITY;
+    }
+}
+
 // One CTA of D threads per (b*h, query row): merge the n_splits summaries.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) fa_splitkv_combine(const float *__restrict__ o_part,
@@ -196,15 +359,49 @@ __global__ void __launch_bounds__(D) fa_splitkv_combine(const float *__restrict_
     if (e == 0) lse[row] = W > 0.f ? M + __logf(W) : -INFINITY;
 }
 
+// Lanes per key row for the several-row kernel: as few as possible (fewer
+// shuffle steps per dot product) while q, acc and two key rows in flight stay
+// near 128 registers, so that four CTAs fit on an SM.
+constexpr int lanes_per_key(int D, int NQ) { return D == 128 ? (NQ <= 4 ? 16 : 32) : (NQ <= 4 ? 8 : 16); }
+
+template <typename T, int D, int NQ>
+int occupancy_d_nq() {
+    int nb = 0;
+    cudaError_t e;
+    if constexpr (NQ == 1)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fa_splitkv_partial<T, D, NQ, false>, kWarpsSK * 32,
+                                                          0);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &nb, fa_splitkv_partial_lg<T, D, NQ, lanes_per_key(D, NQ), false>, kWarpsSK * 32, 0);
+    return e == cudaSuccess && nb > 0 ? nb : 1;
+}
+
+template <int D>
+int occupancy_d(int Nq) {
+    using T = __nv_bfloat16;
+    if (Nq <= 1) return occupancy_d_nq<T, D, 1>();
+    if (Nq <= 2) return occupancy_d_nq<T, D, 2>();
+    if (Nq <= 4) return occupancy_d_nq<T, D, 4>();
+    if (Nq <= 8) return occupancy_d_nq<T, D, 8>();
+    return occupancy_d_nq<T, D, 16>();
+}
+
 template <typename T, int D, int NQ, bool CAUSAL>
 int launch_sk(const SplitKVArgs &a) {
     const int BH = a.B * a.H;
     const int split_len = (a.Nk + a.n_splits - 1) / a.n_splits;
     const float sl2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     dim3 grid(a.n_splits, BH);
-    fa_splitkv_partial<T, D, NQ, CAUSAL><<<grid, kWarpsSK * 32, 0, a.stream>>>(
-        static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v), a.o_part, a.lse_part,
-        BH, a.Nq, a.Nk, split_len, sl2);
+    if constexpr (NQ == 1) {  // one query row: a warp per key row needs no lane groups
+        fa_splitkv_partial<T, D, NQ, CAUSAL><<<grid, kWarpsSK * 32, 0, a.stream>>>(
+            static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v), a.o_part,
+            a.lse_part, BH, a.Nq, a.Nk, split_len, sl2);
+    } else {
+        fa_splitkv_partial_lg<T, D, NQ, lanes_per_key(D, NQ), CAUSAL><<<grid, kWarpsSK * 32, 0, a.stream>>>(
+            static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v), a.o_part,
+            a.lse_part, BH, a.Nq, a.Nk, split_len, sl2);
+    }
     if (cudaGetLastError() != cudaSuccess) return -5;
     fa_splitkv_combine<T, D><<<BH * a.Nq, D, 0, a.stream>>>(a.o_part, a.lse_part, static_cast<T *>(a.out), a.lse,
                                                             BH * a.Nq, a.n_splits);
@@ -228,6 +425,8 @@ int launch_sk_t(const SplitKVArgs &a) {
 }
 
 }  // namespace
+
+int splitkv_blocks_per_sm(int d, int Nq) { return d == 64 ? occupancy_d<64>(Nq) : occupancy_d<128>(Nq); }
 
 int launch_splitkv(const SplitKVArgs &a, bool fp16) {
     return fp16 ? launch_sk_t<__half>(a) : launch_sk_t<__nv_bfloat16>(a);

@@ -29,4 +29,7 @@ inline size_t splitkv_workspace_bytes(int64_t rows, int d, int n_splits) {
 
 int launch_splitkv(const SplitKVArgs &a, bool fp16);
 
+// Resident CTAs per SM of the partial kernel used for (d, Nq) (bf16 variant).
+int splitkv_blocks_per_sm(int d, int Nq);
+
 }  // namespace fa

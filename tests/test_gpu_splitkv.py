@@ -40,7 +40,21 @@ CASES = [
     (2, 2, 16, 20, 128, "bf16", True, 20),   # many empty splits for the early rows
     (1, 2, 9, 5000, 128, "bf16", True, 13),
     (3, 1, 2, 300, 64, "bf16", False, 300),  # one key per split
+    (1, 2, 12, 2000, 64, "bf16", True, None),  # 16-row variant at d = 64 (16 lanes per key row)
+    (2, 2, 4, 8192, 128, "bf16", True, None),  # the four-row decode shape, 8-lane groups
 ]
+
+
+@pytest.mark.parametrize("Nq,d", [(1, 128), (4, 128), (8, 64), (16, 128)])
+def test_splitkv_growing_scores_rescale(fa, Nq, d):
+    """Large scores whose running maximum keeps growing along the keys (Q and K
+    scaled by 3, K rows offset by up to +-4) exercise the lazy rescaling; V stays
+    unit-scale so that the absolute tolerance keeps its meaning."""
+    q, k, _, _ = make_qkv(1, 2, Nq, d, "bf16", seed=50 + Nq, mul=3.0, k_offset=4.0, Nk=6000)
+    _, _, v, _ = make_qkv(1, 2, Nq, d, "bf16", seed=60 + Nq, Nk=6000)
+    out, lse = run(fa, q, k, v, False, 5)
+    ref_o, ref_l = oracle.attention(q, k, v, scale=1 / math.sqrt(d), causal=False)
+    compare(out, lse, ref_o, ref_l)
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d,dtype,causal,n_splits", CASES)
