@@ -444,17 +444,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // overlapped. Each 128-row query block is handled as two 64-row halves h (A =
 // rows 0-63, B = rows 64-127), gradient warpgroup h owning half h, with their
 // own barriers. The tensor core runs, per block i,
-//   dV,dK(A, i)   S,dP(A, i+1)   dV,dK(B, i)   dQ(i)   S,dP(B, i+1)
+//   dV,dK(A, i)   S,dP(A, i+1)   dV,dK(B, i)   S,dP(B, i+1)   dQ(i)
 // so that each warpgroup's P/dS pass of one block overlaps the other half's
-// products (the two warpgroups alternate like a ping-pong). dS is kept in two
-// shared-memory buffers (block parity), because the pass of half A of block
-// i+1 runs before dQ(i) has read dS(i). dQ of block i is read out by the
-// gradient warps after their pass of block i+1 (it has its own tensor-memory
-// columns and its own staging buffer); dQ(i+1) waits for that read-out.
+// products (the two warpgroups alternate like a ping-pong). Nothing the dV
+// and dK products read lives where the next block's S and dP are written:
+// P^T (16 bit) is packed into its own tensor-memory columns, and dK takes
+// dS^T straight from shared memory, where the pass writes dS for dQ anyway
+// (keys as rows, queries contiguous: K-major for dS^T, M-major for dS). So the
+// issuing warp never waits for its own products to finish; a warpgroup's wait
+// for its next S covers every earlier product (a commit tracks all earlier
+// MMAs of the issuing thread), which is when it may overwrite its packed P and
+// its dS buffer. dS is kept in two shared-memory buffers (block parity),
+// because the pass of half A of block i+1 runs before dQ(i) has read dS(i).
+// dQ of block i is read out by the gradient warps after their pass of block
+// i+1 (it has its own tensor-memory columns and its own staging buffer);
+// dQ(i+1) waits for that read-out.
 // Tensor memory: S_A [0,64), dP_A [64,128), S_B [128,192), dP_B [192,256),
-// dV [256,320), dK [320,384), dQ [384,448). Each half's P^T and dS^T are packed
-// into the first 32 columns of its own S and dP ranges (columns its warpgroup
-// has already read).
+// P^T_A [256,288), P^T_B [288,320), dV [320,384), dK [384,448), dQ [448,512).
 template <typename T>
 struct BwdCfgH64 {
     static constexpr int D = 64;
@@ -467,12 +473,12 @@ struct BwdCfgH64 {
     static constexpr int SMEM_STAGE = SMEM_DS + 4 * CHUNK;         // dQ staging: 8 boxes of 32 x 32 fp32
     static constexpr int SMEM_STATS = SMEM_STAGE + 8 * 4096;       // [half][buffer][-lse2 x64, -D x64]
     static constexpr int SMEM_BAR = SMEM_STATS + 2 * 2 * 128 * 4;
-    // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], acc[2], dq_full, dq_free, stats[2], drain
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 1;
+    // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], dq_full, dq_free, stats[2], drain
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
     static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;
     static constexpr uint32_t FMT = Elem<T>::fmt;
     static constexpr uint32_t ID_S = make_idesc_ab(FMT, 128, 64, 0, 0);   // S_h^T, dP_h^T: 128 keys x 64 queries
-    static constexpr uint32_t ID_ACC = make_idesc_ab(FMT, 128, 64, 0, 1); // dV, dK: A in TMEM, B N-major
+    static constexpr uint32_t ID_ACC = make_idesc_ab(FMT, 128, 64, 0, 1); // dV (A in TMEM), dK (A K-major): B N-major
     static constexpr uint32_t ID_DQ = make_idesc_ab(FMT, 128, 64, 1, 1);  // dQ: A M-major, B N-major
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -492,11 +498,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     auto bar_qd_empty = [&](int s) { return smem_u32(bars + 1 + ST + s); };
     auto bar_sp_full = [&](int h) { return smem_u32(bars + 1 + 2 * ST + h); };  // S_h, dP_h computed
     auto bar_p_full = [&](int h) { return smem_u32(bars + 3 + 2 * ST + h); };   // half h packed (128 arrivals)
-    auto bar_acc = [&](int h) { return smem_u32(bars + 5 + 2 * ST + h); };      // dV, dK of half h done
-    const uint32_t bar_dq_full = smem_u32(bars + 7 + 2 * ST);                  // dQ of the block computed
-    const uint32_t bar_dq_free = smem_u32(bars + 8 + 2 * ST);                  // dQ loaded by all (256 arrivals)
-    auto bar_stats = [&](int h) { return smem_u32(bars + 9 + 2 * ST + h); };   // half h statistics (128 arrivals)
-    const uint32_t bar_drain = smem_u32(bars + 11 + 2 * ST);
+    const uint32_t bar_dq_full = smem_u32(bars + 5 + 2 * ST);                  // dQ of the block computed
+    const uint32_t bar_dq_free = smem_u32(bars + 6 + 2 * ST);                  // dQ loaded by all (256 arrivals)
+    auto bar_stats = [&](int h) { return smem_u32(bars + 7 + 2 * ST + h); };   // half h statistics (128 arrivals)
+    const uint32_t bar_drain = smem_u32(bars + 9 + 2 * ST);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -515,7 +520,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar_sp_full(h), 1);
             mbar_init(bar_p_full(h), 128);
-            mbar_init(bar_acc(h), 1);
             mbar_init(bar_stats(h), 128);
         }
         mbar_init(bar_dq_full, 1);
@@ -575,19 +579,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_commit(bar_sp_full(h), issue);
         };
-        // dV_j += P_h^T dO_h, dK_j += dS_h^T Q_h, contracted over the 64 rows of half h of block it
+        // dV_j += P_h^T dO_h (A = packed P^T in TMEM), dK_j += dS_h^T Q_h (A = dS^T, K-major, from the
+        // block's dS buffer), contracted over the 64 rows of half h of block it
         auto issue_acc = [&](int it, int h) {
             const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
             const uint64_t q_mn = smem_desc_sw128(q_s, C::CHUNK, 1024);
             const uint64_t do_mn = smem_desc_sw128(q_s + C::CHUNK, C::CHUNK, 1024);
+            const uint64_t dst_km =
+                smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK + h * C::CHUNK), 16, 1024);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint64_t off = (uint64_t)(((h * 64 + k * 16) * 128) >> 4);
                 const uint32_t acc = (it > 0 || h > 0 || k > 0) ? 1u : 0u;
-                mma_ts(tmem + 256, tmem + 128 * h + 8 * k, do_mn + off, C::ID_ACC, acc, issue);
-                mma_ts(tmem + 320, tmem + 128 * h + 64 + 8 * k, q_mn + off, C::ID_ACC, acc, issue);
+                mma_ts(tmem + 320, tmem + 256 + 32 * h + 8 * k, do_mn + off, C::ID_ACC, acc, issue);
+                mma_ss(tmem + 384, dst_km + (uint64_t)((k * 32) >> 4), q_mn + off, C::ID_ACC, acc, issue);
             }
-            tc_commit(bar_acc(h), issue);
         };
         bool ok = bwd_wait_warp(bar_kv, 0, p) && bwd_wait_warp(bar_qd_full(0), 0, p);
         if (ok) {
@@ -601,11 +607,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             issue_acc(it, 0);
-            if (next) {  // S_A of the next block once dV, dK(A) have read half A's columns
-                ok = bwd_wait_warp(bar_qd_full((it + 1) % ST), ((it + 1) / ST) & 1u, p) &&
-                     bwd_wait_warp(bar_acc(0), it & 1u, p);
+            if (next) {  // half A's S and dP columns were read by its pass: the next block may use them
+                ok = bwd_wait_warp(bar_qd_full((it + 1) % ST), ((it + 1) / ST) & 1u, p);
                 if (!ok) break;
-                tc_fence_after();
                 issue_s(it + 1, 0);
             }
             ok = bwd_wait_warp(bar_p_full(1), it & 1u, p);
@@ -613,6 +617,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             issue_acc(it, 1);
             tc_commit(bar_qd_empty(it % ST), issue);  // every reader of this Q, dO stage is issued
+            if (next) issue_s(it + 1, 1);
             if (it > 0) ok = bwd_wait_warp(bar_dq_free, (it - 1) & 1u, p);  // dQ of the last block read out
             if (!ok) break;
             tc_fence_after();
@@ -622,15 +627,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                mma_ss(tmem + 384, ds_mn + off, k_mn + off, C::ID_DQ, k > 0 ? 1u : 0u, issue);
+                mma_ss(tmem + 448, ds_mn + off, k_mn + off, C::ID_DQ, k > 0 ? 1u : 0u, issue);
             }
             tc_commit(bar_dq_full, issue);
-            if (next) {  // S_B of the next block once dV, dK(B) have read half B's columns
-                ok = bwd_wait_warp(bar_acc(1), it & 1u, p);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(it + 1, 1);
-            }
         }
         tc_commit(bar_drain, issue);
         bwd_wait_warp(bar_drain, 0, p);
@@ -655,7 +654,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!bwd_wait_warp(bar_dq_full, (uint32_t)(blk - i0) & 1u, p)) return false;
             tc_fence_after();
             uint32_t qv[32];
-            tmem_ld32_wait(tmem + lane_base + 384 + 32 * g, qv);
+            tmem_ld32_wait(tmem + lane_base + 448 + 32 * g, qv);
             tc_fence_before();
             mbar_arrive(bar_dq_free);
             stage_and_reduce_dq(&tm_dq, box, qv, p.scale, lane, 32 * g, blk * kBlk + w * 32, bh);
@@ -678,8 +677,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t pp[16], dsp[16];
                 p_ds_chunk<T, CAUSAL>(sv, dpv, stats + c0 * 4, stats + (64 + c0) * 4, p.scale_log2, need_mask,
                                       key_ok, key, i * kBlk + 64 * g + c0, pp, dsp);
-                tmem_st16(s_col + c0 / 2, pp);
-                tmem_st16(s_col + 64 + c0 / 2, dsp);
+                tmem_st16(tmem + lane_base + 256u + 32u * g + c0 / 2, pp);  // packed P^T of half g
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t unit = (uint32_t)((c0 / 8 + u) ^ (r & 7));
@@ -701,7 +699,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float mul = g == 0 ? 1.0f : p.scale;
             T *dst = reinterpret_cast<T *>(g == 0 ? p.dv : p.dk) + ((size_t)bh * p.N + (size_t)(key_ok ? key : 0)) * 64;
             uint32_t a[32], b[32];
-            tmem_ld32x2_wait(tmem + lane_base + 256 + 64 * g, a, tmem + lane_base + 256 + 64 * g + 32, b);
+            tmem_ld32x2_wait(tmem + lane_base + 320 + 64 * g, a, tmem + lane_base + 320 + 64 * g + 32, b);
             if (key_ok) {
 #pragma unroll
                 for (int c = 0; c < 32; c += 8) {

@@ -287,7 +287,7 @@ def simulate_bwd_halves(n_it, stages, seed):
     for name, c in (("kv", 1), ("dq_full", 1), ("dq_free", 256), ("drain", 1)):
         B[name] = Bar(name, c)
     for h in range(2):
-        for name, c in (("sp_full", 1), ("p_full", 128), ("acc", 1), ("stats", 128)):
+        for name, c in (("sp_full", 1), ("p_full", 128), ("stats", 128)):
             B[f"{name}{h}"] = Bar(f"{name}{h}", c)
     for s in range(stages):
         B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
@@ -302,27 +302,25 @@ def simulate_bwd_halves(n_it, stages, seed):
             tma.append(f"qd_full{s}")
 
     def mma():
-        # per block: dV,dK(A, i)  S,dP(A, i+1)  dV,dK(B, i)  dQ(i)  S,dP(B, i+1)
+        # per block: dV,dK(A, i)  S,dP(A, i+1)  dV,dK(B, i)  S,dP(B, i+1)  dQ(i); the issuing warp
+        # never waits for its own products (a warpgroup's wait for its next S covers them)
         yield ("wait", "kv", 0)
         yield ("wait", "qd_full0", 0)
         tensor_pipe.extend([("commit", "sp_full0"), ("commit", "sp_full1")])
         for it in range(n_it):
             nxt = it + 1 < n_it
             yield ("wait", "p_full0", it)
-            tensor_pipe.append(("commit", "acc0"))
             if nxt:
                 s1 = (it + 1) % stages
                 yield ("wait", f"qd_full{s1}", (it + 1) // stages)
-                yield ("wait", "acc0", it)
                 tensor_pipe.append(("commit", "sp_full0"))
             yield ("wait", "p_full1", it)
-            tensor_pipe.extend([("commit", "acc1"), ("commit", f"qd_empty{it % stages}")])
+            tensor_pipe.append(("commit", f"qd_empty{it % stages}"))
+            if nxt:
+                tensor_pipe.append(("commit", "sp_full1"))
             if it > 0:
                 yield ("wait", "dq_free", it - 1)
             tensor_pipe.append(("commit", "dq_full"))
-            if nxt:
-                yield ("wait", "acc1", it)
-                tensor_pipe.append(("commit", "sp_full1"))
         tensor_pipe.append(("commit", "drain"))
         yield ("wait", "drain", 0)
 
