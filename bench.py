@@ -372,6 +372,10 @@ def run_decode(args, w):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     barrier(world, dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -379,6 +383,7 @@ def run_decode(args, w):
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
+    clocks = sampler.stop() if sampler else None
     ms = max_over_ranks(world, a.elapsed_time(b), dev) / args.steps
     if rank != 0:
         return 0
@@ -393,7 +398,8 @@ def run_decode(args, w):
             "gpu_launches": 2 * args.steps,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "peak_source": src, "kernel": "fa_splitkv_partial + fa_splitkv_combine",
-                         "tflops": w.flops / (ms * 1e-3) / 1e12}}
+                         "tflops": w.flops / (ms * 1e-3) / 1e12},
+            "clocks": clocks}
     print(json.dumps(line), flush=True)
     return 0
 
