@@ -6,6 +6,9 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -71,6 +74,25 @@ DeviceInfo *device_info() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// FA_LOG=1 in the environment prints one line per call to stderr: the entry
+// point, the kernel variant it dispatches to and the problem size.
+bool log_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("FA_LOG");
+        return v != nullptr && v[0] != '\0' && v[0] != '0';
+    }();
+    return on;
+}
+void log_call(const char *fmt, ...) {
+    if (!log_enabled()) return;
+    va_list ap;
+    va_start(ap, fmt);
+    std::fputs("[fa] ", stderr);
+    std::vfprintf(stderr, fmt, ap);
+    std::fputc('\n', stderr);
+    va_end(ap);
+}
+
 enum class Type { BF16, FP16, FP32 };
 
 int check_args(Type ty, const void *q, const void *k, const void *v, const float *mask, const void *out,
@@ -95,6 +117,9 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
     if (rc != FA_OK) return rc;
     if (Hkv == -1) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return FA_ERR_SHAPE;
+    log_call("forward %s d=%d causal=%d mask=%d B=%d H=%d Hkv=%d N=%d scale=%g",
+             ty == Type::BF16 ? "bf16 tcgen05" : ty == Type::FP16 ? "fp16 tcgen05" : "fp32 cuda-core", d,
+             causal ? 1 : 0, mask != nullptr, B, H, Hkv, N, static_cast<double>(scale));
     DeviceInfo *di = device_info();
     if (!di || !encoder()) return FA_ERR_LAUNCH;
     fa::LaunchArgs a;
@@ -161,6 +186,8 @@ int splitkv_common(bool fp16, const void *q, const void *k, const void *v, void 
     a.o_part = static_cast<float *>(workspace);
     a.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_bytes);
     a.stream = static_cast<cudaStream_t>(stream);
+    log_call("split-KV %s d=%d causal=%d B=%d H=%d Nq=%d Nk=%d splits=%d", fp16 ? "fp16" : "bf16", d, a.causal, B,
+             H, Nq, Nk, n_splits);
     return fa::launch_splitkv(a, fp16);
 }
 
@@ -198,6 +225,8 @@ int varlen_common(bool fp16, const void *q, const void *k, const void *v, void *
     a.timeout_ns = kDefaultTimeoutNs;
     a.cu_seqlens = cu_seqlens;
     a.total = total;
+    log_call("packed forward %s d=%d causal=%d nseq=%d total=%d max_seqlen=%d H=%d Hkv=%d", fp16 ? "fp16" : "bf16",
+             d, a.causal, nseq, total, max_seqlen, H, Hkv);
     return fp16 ? fa::launch_fwd_varlen_fp16(a) : fa::launch_fwd_varlen_bf16(a);
 }
 
@@ -244,6 +273,8 @@ int bwd_common(bool fp16, const void *q, const void *k, const void *v, const voi
     a.stream = static_cast<cudaStream_t>(stream);
     a.status = di->status;
     a.timeout_ns = kDefaultTimeoutNs;
+    log_call("backward %s d=%d (%s kernel) causal=%d B=%d H=%d N=%d", fp16 ? "fp16" : "bf16", d,
+             d == 64 ? "half-block" : "serial", a.causal, B, H, N);
     return fa::launch_bwd(a, fp16);
 }
 

@@ -50,8 +50,14 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
+    # The mutation tests (tests/test_oracle_mutants.py) point this at a copy of the
+    # oracle built with one planted mistake, to show that the pins catch it.
+    override = os.environ.get("ORACLE_MUTANT_LIB")
+    if override:
+        lib = ctypes.CDLL(override)
+    else:
+        build()
+        lib = ctypes.CDLL(_LIB)
     dp = ctypes.POINTER(ctypes.c_double)
     i64 = ctypes.c_int64
     ip = ctypes.POINTER(ctypes.c_int64)

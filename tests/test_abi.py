@@ -186,3 +186,22 @@ def test_varlen_host_validation(fa, name):
     assert call(H=3, Hkv=2) == fa.FA_ERR_SHAPE
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_status_string(fa.FA_ERR_SEQLENS) != "unknown status"
+
+
+def test_fa_log_prints_the_dispatch_on_the_host(tmp_path):
+    """FA_LOG=1 logs the kernel variant of each call that passes its argument
+    checks (to stderr, before the device is touched: here, without a GPU, the
+    call then fails with FA_ERR_LAUNCH); a call rejected by the checks logs nothing."""
+    import subprocess
+    import sys
+
+    call = ("fa.lib.fa_fwd(ctypes.c_void_p(16), ctypes.c_void_p(32), ctypes.c_void_p(48), None, "
+            "ctypes.c_void_p(64), ctypes.c_void_p(80), 2, 4, 300, {d}, ctypes.c_float(0.1), 1, None)")
+    code = "import ctypes, io_aware_exact_13_gb300.fa as fa; print({a}); print({b})".format(
+        a=call.format(d=96), b=call.format(d=128))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=dict(os.environ, FA_LOG="1"), capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == [str(-4), str(-5)]
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[fa]")]
+    assert len(lines) == 1 and "forward bf16 tcgen05 d=128 causal=1" in lines[0] and "N=300" in lines[0], r.stderr
