@@ -12,7 +12,8 @@ already resident in device memory. Q, K, V and O total 268 MB, more than the
 ranks; each rank runs its own copy of the workload (independent problems, no
 collective on the data path; weak scaling). ``e2e`` is the same metric through
 the C ABI with pinned host buffers: each step copies Q, K, V host->device and
-O, lse device->host inside the timed region. ``roofline`` compares the kernel's
+O, lse device->host inside the timed region, through ``fa_fwd_host`` (the copies
+of one head chunk overlap the forward of another). ``roofline`` compares the kernel's
 algorithmic flops per launch / its CUDA-event duration with the measured dense
 bf16 tensor peak. ``cpu_baseline`` times the fp64 oracle on a bounded sample of
 query rows of the same workload on the host cores (rank 0, N=1 only).
@@ -39,9 +40,9 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, HEADLINE, VARLEN_WORKLOADS,  # noqa: E402
-                                            WORKLOADS, make_bwd, make_decode, make_varlen, make_workload,
-                                            sample_rows)
+from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, GQA_WORKLOADS, HEADLINE,  # noqa: E402
+                                            VARLEN_WORKLOADS, WORKLOADS, make_bwd, make_decode, make_gqa,
+                                            make_varlen, make_workload, sample_rows)
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
 UNIT = "TFLOP/s"
@@ -49,6 +50,7 @@ KERNEL_SOURCES = ["io_aware_exact_13_gb300/csrc/fa_fwd_kernel.cuh", "io_aware_ex
                   "io_aware_exact_13_gb300/csrc/fa_launch.cuh"]
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_BF16_TFLOPS = 1900.0
+E2E_CHUNKS = 4  # head chunks of the pipelined host-memory forward (1.28 ms vs 1.76 ms serial on the headline)
 
 
 def kernel_source_hash() -> str:
@@ -292,7 +294,14 @@ def run_ours(args, w):
     oh = torch.empty(od.shape, dtype=od.dtype).pin_memory()
     lh = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
 
+    # Through the host-memory entry point (copies pipelined with the forward over 4 head chunks) where it
+    # applies (bf16 / fp16, no mask); otherwise copy in, forward, copy out in sequence.
+    host_entry = {"bf16": fa.fa_fwd_host, "fp16": fa.fa_fwd_host}.get(w.dtype) if mh is None else None
+
     def e2e_step():
+        if host_entry is not None:
+            host_entry(qh, kh, vh, oh, lh, qd, kd, vd, od, lsed, w.scale, w.causal, E2E_CHUNKS, stream)
+            return
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
@@ -335,7 +344,9 @@ def run_ours(args, w):
                        parallelism=f"replicas x{world} (independent problems, no collective)"),
         "pct_of_peak": 100.0 * value / (world * peak),
         "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "path": (f"fa_fwd_host, {E2E_CHUNKS} head chunks, copies pipelined with the forward"
+                         if host_entry is not None else "copy in, fa_fwd, copy out")},
         "gpu_launches": args.steps,
         "roofline": roofline,
         "clocks": clocks,
@@ -453,6 +464,59 @@ def run_varlen(args, w):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None, "peak_source": src,
                          "kernel": "fa_fwd_kernel (packed batch)"},
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gqa(args, w):
+    """Grouped-query forward: H query heads over Hkv key/value heads, the persistent forward kernel."""
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from io_aware_exact_13_gb300 import fa
+
+    q, k, v = make_gqa(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    lsed = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    entry = fa.fa_fwd_gqa if w.dtype == "bf16" else fa.fa_fwd_gqa_fp16
+
+    def step():
+        entry(qd, kd, vd, None, od, lsed, w.scale, w.causal, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_get_device_status(stream) != 0:
+        raise SystemExit("device status word set during warm-up")
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world, dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(world, a.elapsed_time(b), dev) / args.steps
+    if rank != 0:
+        return 0
+    peak, src = load_peak()
+    tflops = w.flops() / (ms * 1e-3) / 1e12
+    line = {"metric": "attention fwd TFLOP/s, grouped-query attention", "value": world * tflops, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(w.describe(), workload=args.workload, l2="no flush between steps"),
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_source": src,
+                         "kernel": "fa_fwd_kernel (grouped-query)"},
             "clocks": clocks}
     print(json.dumps(line), flush=True)
     return 0
@@ -589,7 +653,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
                     choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS) + sorted(BWD_WORKLOADS)
-                    + sorted(VARLEN_WORKLOADS))
+                    + sorted(VARLEN_WORKLOADS) + sorted(GQA_WORKLOADS))
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -602,6 +666,8 @@ def main():
         return run_bwd(args, BWD_WORKLOADS[args.workload])
     if args.workload in VARLEN_WORKLOADS:
         return run_varlen(args, VARLEN_WORKLOADS[args.workload])
+    if args.workload in GQA_WORKLOADS:
+        return run_gqa(args, GQA_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -69,6 +69,26 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_o
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                 float *lse, int B, int H, int N, int d, float scale, int causal, void *stream);
 
+/* ---- forward from host memory ---------------------------------------------
+ * The same forward (bf16 / fp16, no mask, Hkv = H) for inputs and outputs in
+ * HOST memory: q_host, k_host, v_host, out_host : [B][H][N][d], lse_host : float
+ * [B][H][N], and caller-owned DEVICE buffers of the same shapes (q_dev .. lse_dev)
+ * that the call uses as staging. The B*H head slabs are cut into n_chunks
+ * (1 .. min(B*H, 64)) contiguous chunks whose host->device copies, forward and
+ * device->host copies are pipelined on two internal copy streams (created on
+ * the first call per device) and `stream`; everything is ordered after earlier
+ * work on `stream` and complete when later work on `stream` starts, so
+ * cudaStreamSynchronize(stream) waits for the results in host memory. Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ * copies to overlap; the results equal fa_fwd's bit for bit. Errors as for
+ * fa_fwd (host pointers must be non-NULL). */
+int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
+                void *q_dev, void *k_dev, void *v_dev, void *out_dev, float *lse_dev, int B, int H, int N, int d,
+                float scale, int causal, int n_chunks, void *stream);
+int fa_fwd_host_fp16(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
+                     void *q_dev, void *k_dev, void *v_dev, void *out_dev, float *lse_dev, int B, int H, int N,
+                     int d, float scale, int causal, int n_chunks, void *stream);
+
 /* ---- grouped-query attention ------------------------------------------------
  * Same operation and layouts as fa_fwd / fa_fwd_fp16, except that k and v hold
  * Hkv heads, [B][Hkv][N][d], each shared by H / Hkv consecutive query heads:

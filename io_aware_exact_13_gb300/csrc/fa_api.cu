@@ -37,6 +37,10 @@ struct DeviceInfo {
     int num_sms = -1;
     int *status = nullptr;
     bool ok = false;
+    // copy streams of the host-buffer entry points (created on first use)
+    std::once_flag streams_once;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    bool streams_ok = false;
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -145,6 +149,101 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
         case Type::FP16: rc = fa::launch_fwd_fp16(a); break;
         case Type::FP32: rc = fa::launch_fwd_fp32(a); break;
     }
+    return rc;
+}
+
+// Forward from host buffers: the B*H head slabs are cut into n_chunks contiguous
+// chunks; chunk c's Q, K, V copies (h2d stream), its forward (the caller's
+// stream) and its O, lse copies (d2h stream) are chained by events, so the
+// copies of one chunk overlap the forward of another.
+int host_common(Type ty, const void *qh, const void *kh, const void *vh, void *oh, float *lh, void *qd, void *kd,
+                void *vd, void *od, float *ld, int B, int H, int N, int d, float scale, int causal, int n_chunks,
+                void *stream) {
+    if (!qh || !kh || !vh || !oh || !lh) return FA_ERR_NULL;
+    int rc = check_args(ty, qd, kd, vd, nullptr, od, ld, B, H, N, d);
+    if (rc != FA_OK) return rc;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (n_chunks < 1 || n_chunks > bh || n_chunks > 64) return FA_ERR_SHAPE;
+    DeviceInfo *di = device_info();
+    if (!di || !encoder()) return FA_ERR_LAUNCH;
+    std::call_once(di->streams_once, [di] {
+        di->streams_ok = cudaStreamCreateWithFlags(&di->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                         cudaStreamCreateWithFlags(&di->d2h, cudaStreamNonBlocking) == cudaSuccess;
+    });
+    if (!di->streams_ok) return FA_ERR_LAUNCH;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const size_t eb = ty == Type::FP32 ? 4 : 2;
+    const size_t slab = static_cast<size_t>(N) * d * eb;  // bytes of one (b, h) slab of Q, K, V or O
+    const size_t lslab = static_cast<size_t>(N) * sizeof(float);
+    cudaEvent_t ev[2 * 64 + 2];
+    int n_ev = 0;
+    auto new_event = [&]() -> cudaEvent_t {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        ev[n_ev++] = e;
+        return e;
+    };
+    rc = FA_OK;
+    cudaEvent_t start = new_event();
+    if (!start || cudaEventRecord(start, cs) != cudaSuccess || cudaStreamWaitEvent(di->h2d, start, 0) != cudaSuccess)
+        rc = FA_ERR_LAUNCH;
+    auto cpy = [](void *dst, const void *src, size_t n, cudaMemcpyKind kind, cudaStream_t st) {
+        return cudaMemcpyAsync(dst, src, n, kind, st) == cudaSuccess;
+    };
+    for (int c = 0; c < n_chunks && rc == FA_OK; ++c) {
+        const int64_t h0 = bh * c / n_chunks, h1 = bh * (c + 1) / n_chunks;
+        const int64_t nh = h1 - h0;
+        const size_t off = static_cast<size_t>(h0) * slab, n = static_cast<size_t>(nh) * slab;
+        const size_t loff = static_cast<size_t>(h0) * lslab, ln = static_cast<size_t>(nh) * lslab;
+        char *qdc = static_cast<char *>(qd) + off, *kdc = static_cast<char *>(kd) + off;
+        char *vdc = static_cast<char *>(vd) + off, *odc = static_cast<char *>(od) + off;
+        float *ldc = reinterpret_cast<float *>(reinterpret_cast<char *>(ld) + loff);
+        cudaEvent_t in_done = new_event(), fwd_done = new_event();
+        if (!in_done || !fwd_done || !cpy(qdc, static_cast<const char *>(qh) + off, n, cudaMemcpyHostToDevice, di->h2d) ||
+            !cpy(kdc, static_cast<const char *>(kh) + off, n, cudaMemcpyHostToDevice, di->h2d) ||
+            !cpy(vdc, static_cast<const char *>(vh) + off, n, cudaMemcpyHostToDevice, di->h2d) ||
+            cudaEventRecord(in_done, di->h2d) != cudaSuccess || cudaStreamWaitEvent(cs, in_done, 0) != cudaSuccess) {
+            rc = FA_ERR_LAUNCH;
+            break;
+        }
+        fa::LaunchArgs a;
+        a.q = qdc;
+        a.k = kdc;
+        a.v = vdc;
+        a.mask = nullptr;
+        a.out = odc;
+        a.lse = ldc;
+        a.B = 1;
+        a.H = static_cast<int>(nh);
+        a.N = N;
+        a.d = d;
+        a.Hkv = static_cast<int>(nh);
+        a.scale = scale;
+        a.causal = causal ? 1 : 0;
+        a.stream = cs;
+        a.status = di->status;
+        a.num_sms = di->num_sms;
+        a.timeout_ns = kDefaultTimeoutNs;
+        int lr = ty == Type::BF16 ? fa::launch_fwd_bf16(a) : fa::launch_fwd_fp16(a);
+        if (lr != 0) {
+            rc = lr;
+            break;
+        }
+        if (cudaEventRecord(fwd_done, cs) != cudaSuccess || cudaStreamWaitEvent(di->d2h, fwd_done, 0) != cudaSuccess ||
+            !cpy(static_cast<char *>(oh) + off, odc, n, cudaMemcpyDeviceToHost, di->d2h) ||
+            !cpy(reinterpret_cast<char *>(lh) + loff, ldc, ln, cudaMemcpyDeviceToHost, di->d2h)) {
+            rc = FA_ERR_LAUNCH;
+            break;
+        }
+    }
+    // the call is complete, on the caller's stream, when the last copy out is
+    cudaEvent_t end = new_event();
+    if (!end || cudaEventRecord(end, di->d2h) != cudaSuccess || cudaStreamWaitEvent(cs, end, 0) != cudaSuccess)
+        rc = rc == FA_OK ? FA_ERR_LAUNCH : rc;
+    for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);  // released once they have completed
+    if (rc == FA_OK)
+        log_call("forward from host %s d=%d causal=%d B=%d H=%d N=%d chunks=%d", ty == Type::BF16 ? "bf16" : "fp16",
+                 d, causal ? 1 : 0, B, H, N, n_chunks);
     return rc;
 }
 
@@ -345,6 +444,20 @@ int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_o
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
                 int B, int H, int N, int d, float scale, int causal, void *stream) {
     return fwd_common(Type::FP32, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
+}
+
+int fa_fwd_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
+                void *q_dev, void *k_dev, void *v_dev, void *out_dev, float *lse_dev, int B, int H, int N, int d,
+                float scale, int causal, int n_chunks, void *stream) {
+    return host_common(Type::BF16, q_host, k_host, v_host, out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev,
+                       B, H, N, d, scale, causal, n_chunks, stream);
+}
+
+int fa_fwd_host_fp16(const void *q_host, const void *k_host, const void *v_host, void *out_host, float *lse_host,
+                     void *q_dev, void *k_dev, void *v_dev, void *out_dev, float *lse_dev, int B, int H, int N, int d,
+                     float scale, int causal, int n_chunks, void *stream) {
+    return host_common(Type::FP16, q_host, k_host, v_host, out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev,
+                       B, H, N, d, scale, causal, n_chunks, stream);
 }
 
 int fa_splitkv_num_splits(int B, int H, int Nq, int Nk, int d) {

@@ -62,6 +62,9 @@ SIGNATURES = {
     "fa_fwd_varlen": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_varlen_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_ulonglong, _vp]),
+    "fa_fwd_host": (ctypes.c_int, [_vp] * 10 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
+    "fa_fwd_host_fp16": (ctypes.c_int, [_vp] * 10 + [ctypes.c_int] * 4 +
+                         [ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp]),
     "fa_bwd_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 4),
     "fa_bwd": (ctypes.c_int, [_vp] * 9 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp,
                                                                  ctypes.c_ulonglong, _vp]),
@@ -147,6 +150,32 @@ def attention(q, k, v, mask=None, scale=None, causal=False, out=None, lse=None, 
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
     return out, lse
+
+
+# ---------------------------------------------------------------- forward from host memory
+def fa_fwd_host(q_host, k_host, v_host, out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev, scale, causal,
+                n_chunks=4, stream=None):
+    """Forward with inputs and outputs in (pinned) host tensors; the device tensors
+    are caller-owned staging buffers. Copies and compute are pipelined over head
+    chunks; synchronise the stream before reading out_host / lse_host."""
+    dtype = q_host.dtype
+    if dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("bf16 or fp16 inputs")
+    for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host), ("out_host", out_host)):
+        if t.dtype != dtype or t.is_cuda or not t.is_contiguous() or t.shape != q_host.shape:
+            raise ValueError(f"{name} must be a contiguous host {dtype} tensor shaped like q_host")
+    for name, t in (("q_dev", q_dev), ("k_dev", k_dev), ("v_dev", v_dev), ("out_dev", out_dev)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous() or t.shape != q_host.shape:
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor shaped like q_host")
+    B, H, N, d = q_host.shape
+    for name, t, cuda in (("lse_host", lse_host, False), ("lse_dev", lse_dev, True)):
+        if t.dtype != torch.float32 or t.is_cuda != cuda or not t.is_contiguous() or t.shape != (B, H, N):
+            raise ValueError(f"{name} must be a contiguous float32 [B, H, N] tensor")
+    fn = lib.fa_fwd_host if dtype == torch.bfloat16 else lib.fa_fwd_host_fp16
+    rc = fn(*[_ptr(t) for t in (q_host, k_host, v_host, out_host, lse_host, q_dev, k_dev, v_dev, out_dev, lse_dev)],
+            B, H, N, d, float(scale), int(bool(causal)), int(n_chunks), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_host")
 
 
 # ---------------------------------------------------------------- grouped-query attention

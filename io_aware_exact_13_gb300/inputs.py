@@ -274,3 +274,41 @@ class VarlenWorkload:
 VARLEN_WORKLOADS = {
     "varlen_t65536_h32_d128_bf16_causal": VarlenWorkload(65536, 256, 8192, 32, 128, "bf16", True, seed=7100),
 }
+
+
+# ---------------------------------------------------------------- grouped-query attention
+@dataclass(frozen=True)
+class GqaWorkload:
+    B: int
+    H: int
+    Hkv: int
+    N: int
+    d: int
+    dtype: str = "bf16"
+    causal: bool = True
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops(self) -> float:
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def describe(self) -> dict:
+        return {"B": self.B, "H": self.H, "Hkv": self.Hkv, "N": self.N, "d": self.d, "dtype": self.dtype,
+                "causal": self.causal}
+
+
+GQA_WORKLOADS = {
+    "gqa_b1h32kv8_n8192_d128_bf16_causal": GqaWorkload(1, 32, 8, 8192, 128, "bf16", True, seed=7200),
+}
+
+
+def make_gqa(w: GqaWorkload):
+    """(q [B, H, N, d], k, v [B, Hkv, N, d]) on the CPU: q drawn by make_qkv with the workload's
+    seed, then k and v by make_qkv with seed + 1 (fp32 normals rounded to the dtype)."""
+    q, _, _, _ = make_qkv(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed)
+    _, k, v, _ = make_qkv(w.B, w.Hkv, w.N, w.d, w.dtype, seed=w.seed + 1)
+    return q, k, v

@@ -205,3 +205,24 @@ def test_fa_log_prints_the_dispatch_on_the_host(tmp_path):
     assert r.stdout.split() == [str(-4), str(-5)]
     lines = [ln for ln in r.stderr.splitlines() if ln.startswith("[fa]")]
     assert len(lines) == 1 and "forward bf16 tcgen05 d=128 causal=1" in lines[0] and "N=300" in lines[0], r.stderr
+
+
+@pytest.mark.parametrize("name", ["fa_fwd_host", "fa_fwd_host_fp16"])
+def test_host_forward_validation(fa, name):
+    f = getattr(fa.lib, name)
+
+    def call(ptrs=None, B=1, H=2, N=16, d=64, chunks=2):
+        p = [0x10000 * (i + 1) for i in range(10)] if ptrs is None else ptrs
+        return f(*[ctypes.c_void_p(x) if x else None for x in p], B, H, N, d, ctypes.c_float(0.125), 0, chunks, None)
+
+    base = [0x10000 * (i + 1) for i in range(10)]
+    for i in range(10):
+        p = list(base)
+        p[i] = 0
+        assert call(p) == fa.FA_ERR_NULL
+    p = list(base)
+    p[6] += 8  # k_dev misaligned
+    assert call(p) == fa.FA_ERR_ALIGN
+    assert call(chunks=0) == fa.FA_ERR_SHAPE
+    assert call(chunks=3) == fa.FA_ERR_SHAPE  # more chunks than B*H = 2
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED

@@ -42,3 +42,25 @@ def test_gqa_matches_repeated_heads(fa, B, H, Hkv, N, d, dtype, causal):
     ref_o, ref_l = oracle.attention(q, k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1),
                                     scale=1 / math.sqrt(d), causal=causal)
     compare(out, lse, ref_o, ref_l)
+
+
+def test_gqa_workload_sampled_heads(fa):
+    """The benchmark's grouped-query workload in the benchmark's launch; the first
+    and last query heads are checked against the oracle run on that head alone
+    (with its K/V head)."""
+    from io_aware_exact_13_gb300.inputs import GQA_WORKLOADS, make_gqa
+
+    w = GQA_WORKLOADS["gqa_b1h32kv8_n8192_d128_bf16_causal"]
+    q, k, v = make_gqa(w)
+    dev = torch.device("cuda")
+    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), None, out, lse, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    g = w.H // w.Hkv
+    for h in (0, w.H - 1):
+        sl = (slice(0, 1), slice(h, h + 1))
+        kv = (slice(0, 1), slice(h // g, h // g + 1))
+        ref_o, ref_l = oracle.attention(q[sl], k[kv], v[kv], scale=w.scale, causal=w.causal)
+        compare(out[sl], lse[sl], ref_o, ref_l)
