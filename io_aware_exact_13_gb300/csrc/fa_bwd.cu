@@ -9,6 +9,11 @@
 // the gradient of sum(dO o O) (D_i = sum_j P_ij dP_ij because the rows of P
 // sum to one).
 //
+// Two kernels share that plan: fa_bwd_kernel_h64 (d = 64, further below), which
+// overlaps the tensor core with the gradient warps over half blocks, and
+// fa_bwd_kernel (used for d = 128, where the dV and dK accumulators leave no
+// tensor memory for that overlap), described here.
+//
 // One CTA owns a 128-key block j of one (b, h) and loops over the 128-row query
 // blocks i that can see it (all of them, or i >= j when causal):
 //   warp 0      TMA: K_j and V_j once, then Q_i and dO_i through a ring
@@ -781,8 +786,11 @@ __global__ void __launch_bounds__(256) fa_bwd_post(const float *__restrict__ dq_
 template <typename T, int D, bool CAUSAL>
 int launch_bwd_variant(const BwdArgs &a) {
     // d = 64 runs the overlapped half-block kernel; d = 128 (tensor memory full) the serial one
-    auto kern = D == 64 ? fa_bwd_kernel_h64<T, CAUSAL> : fa_bwd_kernel<T, D, CAUSAL>;
-    const int smem_bytes = D == 64 ? BwdCfgH64<T>::SMEM_BYTES : BwdCfg<T, D>::SMEM_BYTES;
+    auto kern = [] {
+        if constexpr (D == 64) return fa_bwd_kernel_h64<T, CAUSAL>;
+        else return fa_bwd_kernel<T, D, CAUSAL>;
+    }();
+    constexpr int smem_bytes = D == 64 ? BwdCfgH64<T>::SMEM_BYTES : BwdCfg<T, D>::SMEM_BYTES;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
         return -5;
     const int BH = a.B * a.H;

@@ -14,9 +14,11 @@
 // outputs 5 and 10 with masses 4 and 2 merge to 20/3). A split with no visible
 // key has lse_s = -inf and weight 0; if every split is empty, o = 0, lse = -inf.
 //
-// Decoding reads every key and value once and does ~4d flop per 4d bytes, so the
-// kernel is bound by HBM bandwidth: a warp reads one 128- or 256-byte K row per
-// load instruction (each lane d/32 elements), several rows in flight per lane.
+// Decoding reads every key and value once and does about Nq flop per byte, so
+// the kernels are bound by HBM bandwidth. With one query row a warp reads one
+// 128- or 256-byte K row per load instruction (each lane d/32 elements), several
+// rows in flight per lane, on the CUDA cores; with 2..16 rows the dot products
+// and P V run on 16-row warp-level MMA tiles (fa_splitkv_partial_mma below).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
