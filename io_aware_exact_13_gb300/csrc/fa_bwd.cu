@@ -462,7 +462,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // its dS buffer. dS is kept in two shared-memory buffers (block parity),
 // because the pass of half A of block i+1 runs before dQ(i) has read dS(i).
 // dQ of block i is read out by the gradient warps after their pass of block
-// i+1 (it has its own tensor-memory columns and its own staging buffer);
+// i+1 (it has its own tensor-memory columns; its staging tiles reuse block
+// i's dS buffer, which dK(i) and dQ(i) have finished reading by then);
 // dQ(i+1) waits for that read-out.
 // Tensor memory: S_A [0,64), dP_A [64,128), S_B [128,192), dP_B [192,256),
 // P^T_A [256,288), P^T_B [288,320), dV [320,384), dK [384,448), dQ [448,512).
@@ -470,13 +471,12 @@ template <typename T>
 struct BwdCfgH64 {
     static constexpr int D = 64;
     static constexpr int CHUNK = 128 * 128;          // 128 rows x 128 bytes (one tile at d = 64)
-    static constexpr int STAGES = 2;
+    static constexpr int STAGES = 3;
     static constexpr int SMEM_K = 0;
     static constexpr int SMEM_V = CHUNK;
     static constexpr int SMEM_QD = 2 * CHUNK;                      // STAGES x (Q_i, dO_i)
     static constexpr int SMEM_DS = SMEM_QD + STAGES * 2 * CHUNK;   // dS[2]: queries 0-63 | 64-127, 128 keys each
-    static constexpr int SMEM_STAGE = SMEM_DS + 4 * CHUNK;         // dQ staging: 8 boxes of 32 x 32 fp32
-    static constexpr int SMEM_STATS = SMEM_STAGE + 8 * 4096;       // [half][buffer][-lse2 x64, -D x64]
+    static constexpr int SMEM_STATS = SMEM_DS + 4 * CHUNK;         // [half][buffer][-lse2 x64, -D x64]
     static constexpr int SMEM_BAR = SMEM_STATS + 2 * 2 * 128 * 4;
     // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], dq_full, dq_free, stats[2], drain
     static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
@@ -649,7 +649,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool key_ok = key < p.N;
         const bool ragged_keys = (j + 1) * kBlk > p.N;
         const uint32_t ds_row0 = smem_u32(smem + C::SMEM_DS) + g * C::CHUNK + r * 128;  // + (block & 1) * 32 KB
-        const uint32_t box = smem_u32(smem + C::SMEM_STAGE) + (g * 4 + w) * 4096;
+        // dQ of block b is staged in this warp's own 32 rows of b's dS buffer: dK(b) and dQ(b) have read it by
+        // the time dQ(b) is read out, and this warp writes those rows again only in the pass of block b + 2
+        const uint32_t box0 = smem_u32(smem + C::SMEM_DS) + g * C::CHUNK + w * 4096;  // + (block & 1) * 32 KB
         const uint32_t stats0 = smem_u32(smem + C::SMEM_STATS) + g * 1024;  // + buffer * 512
         // thread r hands over -lse2 (r < 64) or -D (r >= 64) of query row 64g + (r & 63)
         const float *stat_src = (r < 64 ? p.lse2 : p.dsum) + (size_t)bh * p.Npad + 64 * g + (r & 63);
@@ -662,6 +664,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_ld32_wait(tmem + lane_base + 448 + 32 * g, qv);
             tc_fence_before();
             mbar_arrive(bar_dq_free);
+            const uint32_t box = box0 + ((blk - i0) & 1) * 2 * C::CHUNK;
             stage_and_reduce_dq(&tm_dq, box, qv, p.scale, lane, 32 * g, blk * kBlk + w * 32, bh);
             return true;
         };
@@ -675,6 +678,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after();
             const bool need_mask = ragged_keys || (CAUSAL && i == j);
             const uint32_t ds_row = ds_row0 + (it & 1) * 2 * C::CHUNK;
+            // the reduction of dQ(i - 2), staged in these rows, must have read them
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t sv[32], dpv[32];

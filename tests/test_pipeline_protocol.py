@@ -70,4 +70,5 @@ def test_backward_half_block_protocol(n_it):
     from pipeline_model import simulate_bwd_halves
 
     for seed in range(20):
-        assert simulate_bwd_halves(n_it, 2, seed)
+        for stages in (2, 3):
+            assert simulate_bwd_halves(n_it, stages, seed)
