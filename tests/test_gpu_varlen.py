@@ -3,7 +3,6 @@ batch against the oracle run on that sequence alone (attention never crosses
 a sequence boundary)."""
 import math
 
-import numpy as np
 import pytest
 import torch
 
@@ -102,9 +101,9 @@ def test_varlen_bad_bounds_are_skipped_and_reported(fa):
     _check_sequences(q, k, v, cu, out.cpu(), lse.cpu(), 1 / math.sqrt(128), True, seqs=[0, 2])
 
 
-def test_varlen_workload_sampled_sequences(fa):
-    """The benchmark's packed batch in the benchmark's launch; the shortest, the
-    longest and a middle sequence are checked against the oracle."""
+def test_varlen_workload_every_sequence(fa):
+    """The benchmark's packed batch in the benchmark's launch; every sequence is
+    checked against the oracle run on that sequence alone."""
     w = VARLEN_WORKLOADS["varlen_t65536_h32_d128_bf16_causal"]
     L = w.lengths()
     q, k, v, cu = make_varlen(L, w.H, w.H, w.d, w.dtype, seed=w.seed)
@@ -113,6 +112,4 @@ def test_varlen_workload_sampled_sequences(fa):
                                    causal=w.causal)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == fa.FA_OK
-    order = np.argsort(L)
-    _check_sequences(q, k, v, cu, out.cpu(), lse.cpu(), w.scale, w.causal,
-                     seqs=[int(order[0]), int(order[len(L) // 2]), int(order[-1])])
+    _check_sequences(q, k, v, cu, out.cpu(), lse.cpu(), w.scale, w.causal)
