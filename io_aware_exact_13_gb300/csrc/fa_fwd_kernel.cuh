@@ -16,7 +16,8 @@
 //   warp  8     TMA producer: Q tiles once per work item, then K and V rings
 //   warps 9-10  S issuers: S_t = Q_t K^T on tcgen05 for tile t = 0, 1
 //   warps 11-12 PV issuers: O_t += P_t V for tile t = 0, 1
-//   warps 13-15 idle (they complete the last warpgroup)
+//   warp  13    packed batch only: publishes the CTA's work items (see ItemRing)
+//   warps 14-15 idle (they complete the last warpgroup)
 // Each issuing warp runs its loop warp-uniformly and lane 0 issues. Four
 // independent issue streams keep the per-wait and per-instruction issue cost
 // (barrier operations compete with MMA operand reads for shared memory) off
@@ -150,23 +151,106 @@ struct Item {
     int bh, q0, n, tok0;
 };
 
-template <bool VARLEN>
 __device__ __forceinline__ Item get_item(const FwdParams &p, int item) {
     Item it;
     item_coords(p, item, it.bh, it.q0);
     it.n = p.N;
     it.tok0 = 0;
-    if constexpr (VARLEN) {
-        const int s = it.bh / p.H;
-        const int a = __ldg(p.cu_seqlens + s), b = __ldg(p.cu_seqlens + s + 1);
-        // a sequence whose bounds do not fit the batch is skipped (and reported once)
-        const bool bad = a < 0 || b < a || b > p.total || b - a > p.N;
-        if (bad && it.q0 == 0 && (it.bh % p.H) == 0 && threadIdx.x == 0) atomicExch(p.status, kStatusSeqlens);
-        it.n = bad ? 0 : b - a;
-        it.tok0 = bad ? 0 : a;
-    }
     return it;
 }
+
+// Length of packed sequence s, or 0 when its bounds do not fit the batch
+// (such a sequence is skipped and reported once).
+__device__ __forceinline__ int seq_len(const FwdParams &p, int s, int &a, bool &bad) {
+    a = __ldg(p.cu_seqlens + s);
+    const int b = __ldg(p.cu_seqlens + s + 1);
+    bad = a < 0 || b < a || b > p.total || b - a > p.N;
+    return bad ? 0 : b - a;
+}
+
+// Packed batch work list. A grid over nseq x H x ceil(max_seqlen / 256) slots
+// is mostly empty for short sequences, and empty slots unbalance the static
+// schedule. Instead the non-empty items form one compact list, longest first:
+// level l (query rows [256 l, 256 l + 256)) from the top level down, and within
+// a level every sequence longer than 256 l in index order, each with its H
+// heads. A CTA takes list positions in the snake order of item_at. Positions
+// grow monotonically, so a cursor suffices: the current level, its first
+// position and sequence count, and a scan point (rank sequences of the level
+// lie below sequence pos). Counting a level and finding the j-th sequence of a
+// level are warp ballots over 32 sequences at a time; all 32 lanes call.
+struct VarlenCursor {
+    int w = 0, lvl, cnt, start = 0, pos = 0, rank = 0;
+
+    __device__ __forceinline__ static int count_level(const FwdParams &p, int l) {
+        const int thr = l * kRowsPerItem;
+        int c = 0;
+        for (int s0 = 0; s0 < p.B; s0 += 32) {
+            const int s = s0 + (int)(threadIdx.x & 31);
+            int a;
+            bool bad;
+            const bool q = s < p.B && seq_len(p, s, a, bad) > thr;
+            c += __popc(__ballot_sync(0xffffffffu, q));
+        }
+        return c;
+    }
+
+    __device__ __forceinline__ explicit VarlenCursor(const FwdParams &p) {
+        int mx = 0;
+        bool any_bad = false;
+        for (int s0 = 0; s0 < p.B; s0 += 32) {
+            const int s = s0 + (int)(threadIdx.x & 31);
+            int a;
+            bool bad = false;
+            if (s < p.B) mx = max(mx, seq_len(p, s, a, bad));
+            any_bad |= bad;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (__any_sync(0xffffffffu, any_bad) && blockIdx.x == 0 && (threadIdx.x & 31) == 0)
+            atomicExch(p.status, kStatusSeqlens);
+        lvl = mx > 0 ? (mx - 1) / kRowsPerItem : -1;
+        cnt = lvl >= 0 ? count_level(p, lvl) : 0;
+    }
+
+    __device__ __forceinline__ bool next(const FwdParams &p, Item &it) {
+        if (lvl < 0) return false;
+        const int G = gridDim.x;
+        const int c = (w & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+        const int k = w * G + c;  // list positions < B*H*levels, an int
+        ++w;
+        while (k >= start + cnt * p.H) {
+            start += cnt * p.H;
+            if (--lvl < 0) return false;
+            cnt = count_level(p, lvl);
+            pos = 0;
+            rank = 0;
+        }
+        const int r = k - start;
+        const int j = r / p.H, h = r - j * p.H;
+        const int thr = lvl * kRowsPerItem;
+        // the j-th sequence (0-based, index order) with rows at this level
+        for (; pos < p.B; pos += 32) {
+            const int s = pos + (int)(threadIdx.x & 31);
+            int a = 0, n = 0;
+            bool bad;
+            if (s < p.B) n = seq_len(p, s, a, bad);
+            uint32_t bal = __ballot_sync(0xffffffffu, n > thr);
+            const int nb = __popc(bal);
+            if (rank + nb > j) {
+                for (int i = rank; i < j; ++i) bal &= bal - 1u;  // drop the lower set bits
+                const int src = __ffs(bal) - 1;
+                it.bh = (pos + src) * p.H + h;
+                it.q0 = thr;
+                it.n = __shfl_sync(0xffffffffu, n, src);
+                it.tok0 = __shfl_sync(0xffffffffu, a, src);
+                return true;
+            }
+            rank += nb;
+        }
+        lvl = -1;  // not reached while cu_seqlens is unchanged during the launch
+        return false;
+    }
+};
 
 // Number of K/V blocks query tile t of an item must visit.
 template <bool CAUSAL>
@@ -223,6 +307,69 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, p));
 }
 
+// The items of one CTA, in the order every role visits them. All 32 lanes of
+// a warp call next() together; every warp of the CTA sees the same sequence.
+template <bool VARLEN>
+struct ItemIter;
+
+template <>
+struct ItemIter<false> {
+    int w = 0;
+    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *) {}
+    __device__ __forceinline__ bool next(const FwdParams &p, Item &it, bool &) {
+        const int item = item_at(p, w++);
+        if (item < 0) return false;
+        it = get_item(p, item);
+        return true;
+    }
+};
+
+// Packed batch: one otherwise idle warp walks the cursor and publishes each
+// item in a 4-slot ring in shared memory (a descriptor plus a full and an
+// empty barrier per slot); the other roles read it from there, so the issuing
+// warps keep no cursor state and do no scans. A descriptor with bh < 0 ends
+// the list. The 13 consumers are the producer, the four issuing warps and the
+// eight softmax warps (lane 0 of each arrives on the empty barrier).
+constexpr int kItemRing = 4;
+constexpr int kItemConsumers = 13;
+
+struct ItemRing {
+    uint64_t full[kItemRing];
+    uint64_t empty[kItemRing];
+    int4 desc[kItemRing];
+};
+
+__device__ __forceinline__ ItemRing &item_ring() {
+    __shared__ __align__(16) ItemRing ring;
+    return ring;
+}
+
+template <>
+struct ItemIter<true> {
+    uint32_t i = 0;
+    volatile int *abort_flag;
+    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *abort) : abort_flag(abort) {}
+    // false at the end of the list; a wait that gives up also clears ok
+    __device__ __forceinline__ bool next(const FwdParams &p, Item &it, bool &ok) {
+        ItemRing &ring = item_ring();
+        const uint32_t slot = i % kItemRing;
+        if (!wait_warp(smem_u32(&ring.full[slot]), (i / kItemRing) & 1u, abort_flag, p)) {
+            ok = false;
+            return false;
+        }
+        const int4 d = ring.desc[slot];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&ring.empty[slot]));
+        ++i;
+        if (d.x < 0) return false;
+        it.bh = d.x;
+        it.q0 = d.y;
+        it.n = d.z;
+        it.tok0 = d.w;
+        return true;
+    }
+};
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
 template <>
@@ -250,7 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Sync<R> sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    // a static shared word: its address is a constant, so no register holds it
+    __shared__ int abort_word;
+    volatile int *abort_flag = &abort_word;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -273,6 +422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.v_empty(s), 2);
         }
         mbar_init(sy.drain(), 4);  // one commit per issuing warp
+        if constexpr (VARLEN) {
+            ItemRing &ring = item_ring();
+            for (int i = 0; i < kItemRing; ++i) {
+                mbar_init(smem_u32(&ring.full[i]), 1);
+                mbar_init(smem_u32(&ring.empty[i]), kItemConsumers);
+            }
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -322,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pos;
                 return true;
             };
-            for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                const Item itm = get_item<VARLEN>(p, item);
+            ItemIter<VARLEN> iter(p, abort_flag);
+            for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int q0 = itm.q0, cur_bh = itm.bh;
                 // grouped-query attention: kv_group consecutive query heads share one K/V head
                 const int kv_h = (cur_bh % p.H) / p.kv_group;
@@ -386,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t KVT16 = C::KV_TILE >> 4;
             uint32_t qcount = 0, s_issued = 0, kpos = 0;
             bool ok = true;
-            for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                const Item itm = get_item<VARLEN>(p, item);
+            ItemIter<VARLEN> iter(p, abort_flag);
+            for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int nt = tile_nkv<CAUSAL>(itm, t);
                 const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
                 if (nt > 0) {
@@ -431,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t KVT16 = C::KV_TILE >> 4;
             uint32_t g = 0, vpos = 0;
             bool ok = true;
-            for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-                const Item itm = get_item<VARLEN>(p, item);
+            ItemIter<VARLEN> iter(p, abort_flag);
+            for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int nt = tile_nkv<CAUSAL>(itm, t);
                 const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
                 for (int j = 0; ok && j < nmax; ++j, ++vpos) {
@@ -459,6 +615,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             tc_commit(sy.drain(), issue);
+        } else if (VARLEN && warp == 13) {
+            // ---------------------------------------------------------- packed-batch item list
+            // Walks the compact list and publishes one descriptor per item, then an
+            // end marker, each into the next ring slot once all consumers have read
+            // the slot's previous descriptor.
+            ItemRing &ring = item_ring();
+            VarlenCursor cur(p);
+            bool more = true;
+            for (uint32_t i = 0; more; ++i) {
+                Item it;
+                more = cur.next(p, it);
+                const uint32_t slot = i % kItemRing;
+                if (!wait_warp(smem_u32(&ring.empty[slot]), ((i / kItemRing) & 1u) ^ 1u, abort_flag, p)) break;
+                if (lane == 0) {
+                    ring.desc[slot] = more ? make_int4(it.bh, it.q0, it.n, it.tok0) : make_int4(-1, 0, 0, 0);
+                    mbar_arrive(smem_u32(&ring.full[slot]));  // release: the descriptor is visible to waiters
+                }
+                __syncwarp();
+            }
         }
     } else {
         setmaxnreg_inc<200>();
@@ -478,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t scount = 0;  // S blocks consumed (all items)
         uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
         bool ok = true;
-        for (int w = 0, item; ok && (item = item_at(p, w)) >= 0; ++w) {
-            const Item itm = get_item<VARLEN>(p, item);
+        ItemIter<VARLEN> iter(p, abort_flag);
+        for (Item itm; ok && iter.next(p, itm, ok);) {
             const int bh = itm.bh, q0 = itm.q0, n = itm.n;
             const int nt = tile_nkv<CAUSAL>(itm, t);
             if (nt == 0) continue;

@@ -53,12 +53,18 @@ class Deadlock(AssertionError):
 
 
 def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, rescale_prob=0.1,
-             skip_empty_items=True):
+             skip_empty_items=True, item_ring=0, ring_waits_empty=True):
     """Run one CTA's item list (first query rows) to completion; raise Deadlock or
     AssertionError on a protocol fault. ``per_buffer_p=False`` models a single
     P-ready barrier per tile (a protocol that is known to alias);
     ``skip_empty_items=False`` a producer that loads K block 0 even for an item
-    with no rows (known to leave the K ring out of step)."""
+    with no rows (known to leave the K ring out of step).
+
+    ``item_ring`` > 0 models the packed-batch kernel: a scheduler warp publishes
+    each item, then an end marker, into a ring of that many slots (full barrier:
+    one arrival; empty barrier: one arrival per consumer warp), and every role
+    takes its items from the ring. ``ring_waits_empty=False`` is a scheduler
+    that refills a slot without waiting for its readers (it must be caught)."""
     rnd = random.Random(seed)
     B = {}
 
@@ -79,7 +85,23 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
         bar(f"k_empty{s}", 2)
         bar(f"v_full{s}", 1)
         bar(f"v_empty{s}", 2)
+    consumers = 5 + 2 * softmax_warps
+    for s in range(item_ring):
+        bar(f"item_full{s}", 1)
+        bar(f"item_empty{s}", consumers)
     tensor_pipe, tma = [], []
+
+    def take(i):
+        # read list entry i (i == len(items) is the end marker) from the ring
+        if item_ring:
+            yield ("wait", f"item_full{i % item_ring}", i // item_ring)
+            yield ("arrive", f"item_empty{i % item_ring}", 1)
+
+    def scheduler():
+        for i in range(len(items) + 1):
+            if ring_waits_empty:
+                yield ("wait", f"item_empty{i % item_ring}", i // item_ring - 1)
+            yield ("arrive", f"item_full{i % item_ring}", 1)
 
     def p_full_name(t, g):
         return (f"p_full{t}{g & 1}", g >> 1) if per_buffer_p else (f"p_full{t}", g)
@@ -92,7 +114,8 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
 
     def producer():
         qcount, kpos, vpos = [0, 0], 0, 0
-        for q0 in items:
+        for i, q0 in enumerate(items):
+            yield from take(i)
             n, nmax = counts(q0)
             for t in range(2):
                 if n[t]:
@@ -110,10 +133,12 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
                     yield ("wait", f"v_empty{vpos % ring}", vpos // ring - 1)
                     tma.append(f"v_full{vpos % ring}")
                     vpos += 1
+        yield from take(len(items))
 
     def s_issuer(t):
         qcount = issued = kpos = 0
-        for q0 in items:
+        for i, q0 in enumerate(items):
+            yield from take(i)
             n, nmax = counts(q0)
             if n[t]:
                 yield ("wait", f"q_full{t}", qcount)
@@ -130,10 +155,12 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
                 issued += 1
                 tensor_pipe.extend([("commit", f"s_full{t}")] + ([("commit", f"q_empty{t}")] if j == n[t] - 1 else [])
                                    + [("commit", f"k_empty{s}")])
+        yield from take(len(items))
 
     def pv_issuer(t):
         g = vpos = 0
-        for q0 in items:
+        for i, q0 in enumerate(items):
+            yield from take(i)
             n, nmax = counts(q0)
             for j in range(nmax):
                 s = vpos % ring
@@ -145,10 +172,12 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
                 yield ("wait",) + p_full_name(t, g)
                 tensor_pipe.extend([("commit", f"pv_done{t}{g & 1}"), ("commit", f"v_empty{s}")])
                 g += 1
+        yield from take(len(items))
 
     def softmax(t):
         scount = g = 0
-        for q0 in items:
+        for i, q0 in enumerate(items):
+            yield from take(i)
             n, _ = counts(q0)
             if not n[t]:
                 continue
@@ -163,9 +192,12 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
                 yield ("arrive", p_full_name(t, g)[0], BQ // softmax_warps)
                 g += 1
             yield ("wait", f"pv_done{t}{(g - 1) & 1}", (g - 1) >> 1)  # epilogue
+        yield from take(len(items))
 
     agents = {"producer": producer(), "S0": s_issuer(0), "S1": s_issuer(1), "PV0": pv_issuer(0),
               "PV1": pv_issuer(1)}
+    if item_ring:
+        agents["scheduler"] = scheduler()
     for t in range(2):
         for w in range(softmax_warps):
             agents[f"softmax{t}.{w}"] = softmax(t)

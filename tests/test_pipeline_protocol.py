@@ -72,3 +72,32 @@ def test_backward_half_block_protocol(n_it):
     for seed in range(20):
         for stages in (2, 3):
             assert simulate_bwd_halves(n_it, stages, seed)
+
+
+def _packed_items(lengths):
+    """The compact packed-batch list (longest first, no empty items)."""
+    top = (max(lengths) + ROWS - 1) // ROWS
+    return [(qb * ROWS, L) for qb in range(top - 1, -1, -1) for L in lengths if L > qb * ROWS]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("ring", [2, 5])
+@pytest.mark.parametrize("item_ring", [1, 2, 4])
+def test_packed_batch_item_ring(causal, ring, item_ring):
+    """Items handed from the scheduler warp to the 13 consumer warps through the
+    ring: no deadlock, no aliased parity wait, for short and empty lists."""
+    for lengths in ([1000, 1, 300, 64, 257], [5], [128, 129]):
+        for seed in range(6):
+            assert simulate(max(lengths), causal, _packed_items(lengths), ring, seed, item_ring=item_ring)
+    assert simulate(16, causal, [], ring, 0, item_ring=item_ring)  # end marker only
+
+
+def test_item_ring_without_empty_wait_is_caught():
+    caught = 0
+    for seed in range(10):
+        try:
+            simulate(2000, True, _packed_items([2000, 700, 300, 1500]), 5, seed, item_ring=2,
+                     ring_waits_empty=False)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
