@@ -50,7 +50,7 @@ KERNEL_SOURCES = ["io_aware_exact_13_gb300/csrc/fa_fwd_kernel.cuh", "io_aware_ex
                   "io_aware_exact_13_gb300/csrc/fa_launch.cuh"]
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_BF16_TFLOPS = 1900.0
-E2E_CHUNKS = 4  # head chunks of the pipelined host-memory forward (1.28 ms vs 1.76 ms serial on the headline)
+E2E_CHUNKS = 4  # head chunks of the pipelined host-memory forward (1.24 ms vs 1.76 ms serial on the headline)
 
 
 def kernel_source_hash() -> str:

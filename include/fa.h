@@ -74,7 +74,10 @@ int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_o
  * HOST memory: q_host, k_host, v_host, out_host : [B][H][N][d], lse_host : float
  * [B][H][N], and caller-owned DEVICE buffers of the same shapes (q_dev .. lse_dev)
  * that the call uses as staging. The B*H head slabs are cut into n_chunks
- * (1 .. min(B*H, 64)) contiguous chunks whose host->device copies, forward and
+ * (1 .. min(B*H, 64)) contiguous chunks, shrinking toward the end in the ratio
+ * n_chunks : n_chunks-1 : ... : 1 (rounded to whole heads; a chunk that rounds
+ * to none is skipped) so that the last forward and copy-out, which no copy
+ * overlaps, are short. Each chunk's host->device copies, forward and
  * device->host copies are pipelined on two internal copy streams (created on
  * the first call per device) and `stream`; everything is ordered after earlier
  * work on `stream` and complete when later work on `stream` starts, so

@@ -190,9 +190,15 @@ int host_common(Type ty, const void *qh, const void *kh, const void *vh, void *o
     auto cpy = [](void *dst, const void *src, size_t n, cudaMemcpyKind kind, cudaStream_t st) {
         return cudaMemcpyAsync(dst, src, n, kind, st) == cudaSuccess;
     };
+    // Chunk sizes shrink linearly (n_chunks : n_chunks-1 : ... : 1): the link is
+    // the bound, and the last chunk's forward and copy-out, which no copy in
+    // overlaps, should be short. cum(c) = sum of the first c weights.
+    const int64_t wsum = static_cast<int64_t>(n_chunks) * (n_chunks + 1) / 2;
+    auto cum = [n_chunks](int64_t c) { return c * n_chunks - c * (c - 1) / 2; };
     for (int c = 0; c < n_chunks && rc == FA_OK; ++c) {
-        const int64_t h0 = bh * c / n_chunks, h1 = bh * (c + 1) / n_chunks;
+        const int64_t h0 = bh * cum(c) / wsum, h1 = bh * cum(c + 1) / wsum;
         const int64_t nh = h1 - h0;
+        if (nh == 0) continue;  // a chunk that rounds to no head
         const size_t off = static_cast<size_t>(h0) * slab, n = static_cast<size_t>(nh) * slab;
         const size_t loff = static_cast<size_t>(h0) * lslab, ln = static_cast<size_t>(nh) * lslab;
         char *qdc = static_cast<char *>(qd) + off, *kdc = static_cast<char *>(kd) + off;

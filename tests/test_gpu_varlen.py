@@ -113,3 +113,32 @@ def test_varlen_workload_every_sequence(fa):
     torch.cuda.synchronize()
     assert fa.fa_get_device_status() == fa.FA_OK
     _check_sequences(q, k, v, cu, out.cpu(), lse.cpu(), w.scale, w.causal)
+
+
+def test_varlen_many_sequences_and_levels(fa):
+    """More sequences than a warp ballot covers (the item list scans them 32 at a
+    time), zero lengths among them, lengths over several 256-row levels, and
+    grouped K/V heads: every sequence against the oracle."""
+    g = torch.Generator().manual_seed(21)
+    lengths = [int(x) for x in torch.randint(0, 1500, (100,), generator=g)]
+    lengths[5] = lengths[40] = lengths[99] = 0
+    lengths[63] = 1500
+    q, k, v, cu = make_varlen(lengths, 3, 1, 64, "bf16", seed=22)
+    dev = torch.device("cuda")
+    out, lse = fa.attention_varlen(q.to(dev), k.to(dev), v.to(dev), cu.to(dev), max(lengths), causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    _check_sequences(q, k, v, cu, out.cpu(), lse.cpu(), 1 / math.sqrt(64), True)
+
+
+def test_varlen_all_sequences_empty(fa):
+    """Every sequence has length 0: no work item, nothing written, no error."""
+    q, k, v, _ = make_varlen([16], 2, 2, 128, "bf16", seed=23)
+    cu = torch.zeros(5, dtype=torch.int32)
+    dev = torch.device("cuda")
+    out = torch.full(q.shape, 5.0, dtype=q.dtype, device=dev)
+    lse = torch.full((2, q.shape[0]), 5.0, dtype=torch.float32, device=dev)
+    fa.fa_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), out, lse, cu.to(dev), 16, 0.1, True)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert torch.all(out == 5.0) and torch.all(lse == 5.0)
