@@ -33,6 +33,12 @@
 namespace fa {
 namespace {
 
+// Programmatic dependent launch: a CTA of the producing kernel lets the
+// dependent grid be scheduled; the dependent waits until every CTA of the
+// producing grid has finished and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr int kWarpsSK = 4;
 constexpr int kUnroll = 4;  // key rows in flight per lane
 
@@ -83,6 +89,7 @@ __global__ void __launch_bounds__(kWarpsSK * 32) fa_splitkv_partial(const T *__r
                                                                     float *__restrict__ lse_part, int BH, int Nq,
                                                                     int Nk, int split_len, float scale_log2) {
     constexpr int E = D / 32;
+    grid_launch_dependents();
     const int split = blockIdx.x, bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k0 = split * split_len, k1 = min(Nk, k0 + split_len);
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(kWarpsSK * 32) fa_splitkv_partial_mma(
     constexpr int KS = D / 16;               // k-steps of S over the head dimension
     constexpr int NT = D / 8;                // n-tiles of O over the head dimension
     extern __shared__ __align__(128) uint8_t sm_raw[];
+    grid_launch_dependents();
     const int split = blockIdx.x, bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -377,10 +385,13 @@ __global__ void __launch_bounds__(kWarpsSK * 32) fa_splitkv_partial_mma(
 }
 
 // One CTA of D threads per (b*h, query row): merge the n_splits summaries.
+// Launched as a programmatic dependent of the partial kernel: its CTAs may be
+// scheduled while the partial kernel drains and wait here for all its results.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) fa_splitkv_combine(const float *__restrict__ o_part,
                                                        const float *__restrict__ lse_part, T *__restrict__ out,
                                                        float *__restrict__ lse, int rows, int n_splits) {
+    grid_dependency_wait();
     const int row = blockIdx.x;  // (b*h)*Nq + i
     const int e = threadIdx.x;
     float M = -INFINITY;
@@ -439,8 +450,21 @@ int launch_sk(const SplitKVArgs &a) {
                                                       a.Nk, split_len, sl2);
     }
     if (cudaGetLastError() != cudaSuccess) return -5;
-    fa_splitkv_combine<T, D><<<BH * a.Nq, D, 0, a.stream>>>(a.o_part, a.lse_part, static_cast<T *>(a.out), a.lse,
-                                                            BH * a.Nq, a.n_splits);
+    // programmatic dependent launch: the combine's launch overlaps the partial kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH * a.Nq);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fa_splitkv_combine<T, D>, static_cast<const float *>(a.o_part),
+                           static_cast<const float *>(a.lse_part), static_cast<T *>(a.out), a.lse, BH * a.Nq,
+                           a.n_splits) != cudaSuccess)
+        return -5;
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
