@@ -50,6 +50,7 @@
 
 #include "fa_bwd.cuh"
 #include "fa_launch.cuh"
+#include "pdl.cuh"
 
 namespace fa {
 namespace {
@@ -116,6 +117,16 @@ __device__ __forceinline__ uint32_t pk2(float lo, float hi) {
     } else {
         __half2 h = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+// Two packed 16-bit values -> (low, high) as floats.
+template <typename T>
+__device__ __forceinline__ float2 up2(uint32_t v) {
+    if constexpr (Elem<T>::fmt == 1) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&v));
+    } else {
+        return __half22float2(*reinterpret_cast<__half2 *>(&v));
     }
 }
 
@@ -205,6 +216,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_qblk = p.Npad / kBlk;
     const int i0 = CAUSAL ? j : 0;  // first query block that sees key block j
     const int n_it = n_qblk - i0;   // >= 1
+    grid_launch_dependents();       // fa_bwd_post may be scheduled once every CTA has started
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv, 1);
@@ -326,6 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t stage = ds_base + g * C::CHUNK + w * 4096;
         // one statistic per thread: -lse2 (group 0) or -D (group 1) of query row r of the block
         const float *stat_src = (g == 0 ? p.lse2 : p.dsum) + (size_t)bh * p.Npad + r;
+        grid_dependency_wait();  // statistics and the zeroed dQ accumulator are written by fa_bwd_pre
         float stat_next = -__ldg(stat_src + i0 * kBlk);
         const bool ragged_keys = (j + 1) * kBlk > p.N;
         bool ok = true;
@@ -515,6 +528,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_qblk = p.Npad / kBlk;
     const int i0 = CAUSAL ? j : 0;
     const int n_it = n_qblk - i0;  // >= 1
+    grid_launch_dependents();      // fa_bwd_post may be scheduled once every CTA has started
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv, 1);
@@ -655,6 +669,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t stats0 = smem_u32(smem + C::SMEM_STATS) + g * 1024;  // + buffer * 512
         // thread r hands over -lse2 (r < 64) or -D (r >= 64) of query row 64g + (r & 63)
         const float *stat_src = (r < 64 ? p.lse2 : p.dsum) + (size_t)bh * p.Npad + 64 * g + (r & 63);
+        grid_dependency_wait();  // statistics and the zeroed dQ accumulator are written by fa_bwd_pre
         float stat_next = -__ldg(stat_src + i0 * kBlk);
         bool ok = true;
         auto readout = [&](int blk) -> bool {  // dQ rows of query block blk, head columns 32g..32g+31
@@ -735,51 +750,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
-// Row statistics for the backward, one warp per padded row:
+// Row statistics for the backward:
 //   dsum = sum_t dO_t O_t (0 past N), lse2 = lse * log2(e) (+inf past N),
-// and the row's dQ accumulator is zeroed.
+// and the row's dQ accumulator is zeroed. D / 8 consecutive threads share a
+// padded row, each with 8 elements (one 16-byte load of O and of dO, two
+// 16-byte stores of zeros); the row sum is a shuffle tree within the group.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre(const T *__restrict__ out, const T *__restrict__ dout,
                                                   const float *__restrict__ lse, float *__restrict__ lse2,
                                                   float *__restrict__ dsum, float *__restrict__ dq_acc, int BH,
                                                   int N, int Npad) {
-    const int64_t prow = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (prow >= (int64_t)BH * Npad) return;
-    const int64_t bh = prow / Npad;
-    const int i = (int)(prow - bh * Npad);
-    if (i >= N) {
-        if (lane == 0) {
-            lse2[prow] = INFINITY;
-            dsum[prow] = 0.0f;
-        }
-        return;
-    }
+    constexpr int TPR = D / 8;          // threads per row (8 or 16: a power of two dividing 32)
+    constexpr int RPB = 256 / TPR;      // rows per CTA
+    grid_launch_dependents();
+    const int64_t prow = (int64_t)blockIdx.x * RPB + threadIdx.x / TPR;
+    const int t = threadIdx.x % TPR;
+    const bool in = prow < (int64_t)BH * Npad;
+    const int64_t bh = in ? prow / Npad : 0;
+    const int i = in ? (int)(prow - bh * Npad) : 0;
+    const bool real = in && i < N;
     const int64_t row = bh * N + i;
     float acc = 0.f;
+    if (real) {
+        const uint4 o = *reinterpret_cast<const uint4 *>(out + row * D + t * 8);
+        const uint4 g = *reinterpret_cast<const uint4 *>(dout + row * D + t * 8);
+        const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int e = lane; e < D; e += 32) {
-        float o, g;
-        if constexpr (Elem<T>::fmt == 1) {
-            o = __bfloat162float(out[row * D + e]);
-            g = __bfloat162float(dout[row * D + e]);
-        } else {
-            o = __half2float(out[row * D + e]);
-            g = __half2float(dout[row * D + e]);
+        for (int u = 0; u < 4; ++u) {
+            const float2 of = up2<T>(ov[u]), gf = up2<T>(gv[u]);
+            acc = fmaf(of.x, gf.x, acc);
+            acc = fmaf(of.y, gf.y, acc);
         }
-        acc = fmaf(o, g, acc);
-        dq_acc[row * D + e] = 0.f;
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + row * D + t * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // every lane takes part (rows past the end contribute 0); xor < TPR stays within the row's group
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        dsum[prow] = acc;
-        lse2[prow] = lse[row] * 1.4426950408889634f;
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (in && t == 0) {
+        dsum[prow] = real ? acc : 0.0f;
+        lse2[prow] = real ? lse[row] * 1.4426950408889634f : INFINITY;
     }
 }
 
+// dQ accumulator -> output type; launched as a programmatic dependent of the
+// backward kernel, whose reductions into the accumulator it waits for.
 template <typename T>
 __global__ void __launch_bounds__(256) fa_bwd_post(const float *__restrict__ dq_acc, T *__restrict__ dq, size_t n4) {
+    grid_dependency_wait();
     const size_t i = (size_t)blockIdx.x * 256 + threadIdx.x;
     if (i >= n4) return;
     const float4 v = reinterpret_cast<const float4 *>(dq_acc)[i];
@@ -802,7 +821,8 @@ int launch_bwd_variant(const BwdArgs &a) {
     const int BH = a.B * a.H;
     const int Npad = static_cast<int>(bwd_padded_rows(a.N));
     const int64_t prows = static_cast<int64_t>(BH) * Npad;
-    fa_bwd_pre<T, D><<<static_cast<unsigned>((prows + 7) / 8), 256, 0, a.stream>>>(
+    constexpr int kPreRows = 256 / (D / 8);  // padded rows per CTA of fa_bwd_pre
+    fa_bwd_pre<T, D><<<static_cast<unsigned>((prows + kPreRows - 1) / kPreRows), 256, 0, a.stream>>>(
         static_cast<const T *>(a.out), static_cast<const T *>(a.dout), a.lse, a.lse2, a.dsum, a.dq_acc, BH, a.N,
         Npad);
     if (cudaGetLastError() != cudaSuccess) return -5;
@@ -827,11 +847,15 @@ int launch_bwd_variant(const BwdArgs &a) {
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
     const int64_t grid = static_cast<int64_t>(BH) * (Npad / kBlk);
-    kern<<<static_cast<unsigned>(grid), kBwdThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo, tdq, p);
-    if (cudaGetLastError() != cudaSuccess) return -5;
+    // programmatic dependents: the backward's copies of K, V, Q, dO start while fa_bwd_pre drains (its
+    // gradient warps wait for the statistics), and fa_bwd_post's launch overlaps the backward's tail
+    if (launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), smem_bytes, a.stream, tq, tk,
+                         tv, tdo, tdq, p) != cudaSuccess)
+        return -5;
     const size_t n4 = static_cast<size_t>(BH) * a.N * D / 4;
-    fa_bwd_post<T><<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dq_acc, static_cast<T *>(a.dq),
-                                                                                   n4);
+    if (launch_dependent(fa_bwd_post<T>, dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, a.stream,
+                         static_cast<const float *>(a.dq_acc), static_cast<T *>(a.dq), n4) != cudaSuccess)
+        return -5;
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

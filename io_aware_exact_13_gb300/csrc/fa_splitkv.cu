@@ -27,17 +27,12 @@
 #include <type_traits>
 
 #include "fa_splitkv.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "warp_mma.cuh"
 
 namespace fa {
 namespace {
-
-// Programmatic dependent launch: a CTA of the producing kernel lets the
-// dependent grid be scheduled; the dependent waits until every CTA of the
-// producing grid has finished and its memory operations are visible.
-__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 constexpr int kWarpsSK = 4;
 constexpr int kUnroll = 4;  // key rows in flight per lane
@@ -451,19 +446,9 @@ int launch_sk(const SplitKVArgs &a) {
     }
     if (cudaGetLastError() != cudaSuccess) return -5;
     // programmatic dependent launch: the combine's launch overlaps the partial kernel's tail
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(BH * a.Nq);
-    cfg.blockDim = dim3(D);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fa_splitkv_combine<T, D>, static_cast<const float *>(a.o_part),
-                           static_cast<const float *>(a.lse_part), static_cast<T *>(a.out), a.lse, BH * a.Nq,
-                           a.n_splits) != cudaSuccess)
+    if (launch_dependent(fa_splitkv_combine<T, D>, dim3(BH * a.Nq), dim3(D), 0, a.stream,
+                         static_cast<const float *>(a.o_part), static_cast<const float *>(a.lse_part),
+                         static_cast<T *>(a.out), a.lse, BH * a.Nq, a.n_splits) != cudaSuccess)
         return -5;
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
