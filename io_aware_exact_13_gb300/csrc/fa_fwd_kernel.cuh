@@ -74,7 +74,10 @@ struct Elem<__half> {
     static constexpr CUtensorMapDataType tma = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 };
 
-template <typename T, int D>
+// MASK: each softmax warp stages the next key block's mask values for its 32
+// rows in shared memory (8 KB per warp, 32 KB per query tile), taken from the
+// K/V rings' share.
+template <typename T, int D, bool MASK = false>
 struct Cfg {
     static constexpr int EB = sizeof(T);
     static constexpr int ROW_BYTES = D * EB;                // one row of Q/K/V
@@ -92,11 +95,14 @@ struct Cfg {
     // shared memory: Q0 Q1 | K ring | V ring | barriers
     static constexpr int SMEM_Q = 0;
     static constexpr int SMEM_KV = 2 * Q_TILE;
-    static constexpr int RING_FREE = 232448 - 1024 - 512 - SMEM_KV;
+    static constexpr int MASK_TILE = kBQ * kBK * 4;           // 128 rows x 64 fp32 mask values
+    static constexpr int MASK_BYTES = MASK ? 2 * MASK_TILE : 0;
+    static constexpr int RING_FREE = 232448 - 1024 - 512 - SMEM_KV - MASK_BYTES;
     static constexpr int RING = (RING_FREE / KV_TILE / 2) > 6 ? 6 : (RING_FREE / KV_TILE / 2);  // slots per ring
     static constexpr int STAGES = 2 * RING;
     static constexpr int SMEM_V = SMEM_KV + RING * KV_TILE;
-    static constexpr int SMEM_BAR = SMEM_KV + STAGES * KV_TILE;
+    static constexpr int SMEM_MASK = SMEM_KV + STAGES * KV_TILE;
+    static constexpr int SMEM_BAR = SMEM_MASK + MASK_BYTES;
     // q_full[2] q_empty[2] k_full[R] k_empty[R] v_full[R] v_empty[R] s_full[2] s_free[2] p_full[2][2]
     // pv_done[2][2] drain
     static constexpr int NUM_BARS = 2 + 2 + 4 * RING + 2 + 2 + 4 + 4 + 1;
@@ -122,6 +128,7 @@ struct FwdParams {
     const int *cu_seqlens;  // [B + 1] token offsets of the sequences
     int total;              // tokens in the batch
     int Hkv;                // key/value heads
+    int mask_tma;           // 1: the mask tensor map is valid (N % 4 == 0) and mask blocks arrive by TMA
 };
 
 // Static schedule: CTA c takes item w*G + c in even waves w and w*G + (G-1-c)
@@ -339,6 +346,12 @@ struct ItemRing {
     int4 desc[kItemRing];
 };
 
+// Masked variant: one mbarrier per softmax warp for its mask copies.
+__device__ __forceinline__ uint64_t *mask_bars() {
+    __shared__ uint64_t bars[8];
+    return bars;
+}
+
 __device__ __forceinline__ ItemRing &item_ring() {
     __shared__ __align__(16) ItemRing ring;
     return ring;
@@ -389,9 +402,10 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
 template <typename T, int D, bool CAUSAL, bool HAS_MASK, bool VARLEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_m,
+                  const FwdParams p) {
     static_assert(!(VARLEN && HAS_MASK), "no mask in a packed batch");
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, HAS_MASK>;
     constexpr int R = C::RING;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,6 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.v_empty(s), 2);
         }
         mbar_init(sy.drain(), 4);  // one commit per issuing warp
+        if constexpr (HAS_MASK) {
+            for (int w = 0; w < 8; ++w) mbar_init(smem_u32(mask_bars() + w), 1);
+        }
         if constexpr (VARLEN) {
             ItemRing &ring = item_ring();
             for (int i = 0; i < kItemRing; ++i) {
@@ -640,6 +657,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------------- softmax + epilogue
         const int t = warp >> 2;                   // query tile of this warpgroup
         const int r = threadIdx.x & 127;           // row within the tile = TMEM lane
+        // mask staging area of this warp (masked variant only): two 32-row x 128-byte TMA boxes
+        const uint32_t mwarp = smem_u32(smem + C::SMEM_MASK + t * C::MASK_TILE + (warp & 3) * 8192);
+        const uint64_t mpol = policy_evict_last();  // the mask is shared by every head of a batch index
+        uint32_t mcount = 0;    // mask blocks consumed by this warp (parity of its barrier)
+        bool mpending = false;  // a mask copy is in flight
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + t * 64;
         const uint32_t p_addr = tmem + lane_base + 128 + t * 64;
@@ -660,6 +682,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nt == 0) continue;
             const int row = q0 + t * kBQ + r;  // global query row (may be >= N in a ragged tail)
             const int b = bh / p.H;
+            // HAS_MASK (mask_tma): the warp's 32 rows x 64 mask values of a key block arrive by two TMA
+            // boxes (32 rows x 32 fp32, 128-byte swizzle; rows past N and keys past N read as 0) into the
+            // warp's 8 KB staging area, issued while the block before it is processed
+            const int mrow0 = q0 + t * kBQ + (warp & 3) * 32;
+            auto stage_mask = [&](int jj) {  // all 32 lanes
+                fence_proxy_async_smem();  // this lane's reads of the area come before the copy's writes
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t bar = smem_u32(mask_bars() + warp);
+                    mbar_arrive_expect_tx(bar, 2 * 32 * 128);
+                    tma_load_3d(mwarp, &tm_m, bar, jj * kBK, mrow0, b, mpol);
+                    tma_load_3d(mwarp + 4096, &tm_m, bar, jj * kBK + 32, mrow0, b, mpol);
+                }
+                __syncwarp();
+                mpending = true;
+            };
+            if constexpr (HAS_MASK) {
+                if (p.mask_tma && nt > 0) stage_mask(0);
+            }
             float m_ref = -INFINITY, l = 0.0f;
             for (int j = 0; j < nt; ++j, ++g) {
                 ok = wait_warp(sy.s_full(t), scount & 1u, abort_flag, p);
@@ -676,16 +717,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (HAS_MASK) {
                     const bool row_ok = row < p.N;
                     const float *mrow = p.mask + ((size_t)b * p.N + (size_t)(row_ok ? row : 0)) * p.N + kbase;
-                    const bool vec = row_ok && ((p.N & 3) == 0) && (kbase + kBK <= p.N);
-                    if (vec) {
+                    if (p.mask_tma) {  // warp-uniform
+                        ok = wait_warp(smem_u32(mask_bars() + warp), mcount & 1u, abort_flag, p);
+                        if (!ok) break;
+                        ++mcount;
+                        mpending = false;
 #pragma unroll
                         for (int c = 0; c < 64; c += 4) {
-                            const float4 mv = ld_global_nc_v4(mrow + c);
+                            // float c of this row: box c / 32, 16-byte chunk (c % 32) / 4 swizzled by row
+                            const uint32_t chunk = (uint32_t)((c & 31) >> 2) ^ (uint32_t)(lane & 7);
+                            const float4 mv =
+                                ld_shared_v4f(mwarp + (uint32_t)((c >> 5) * 4096 + lane * 128) + (chunk << 4));
                             x[c + 0] = fmaf(__uint_as_float(sr[c + 0]), scale_log2, mv.x * 1.4426950408889634f);
                             x[c + 1] = fmaf(__uint_as_float(sr[c + 1]), scale_log2, mv.y * 1.4426950408889634f);
                             x[c + 2] = fmaf(__uint_as_float(sr[c + 2]), scale_log2, mv.z * 1.4426950408889634f);
                             x[c + 3] = fmaf(__uint_as_float(sr[c + 3]), scale_log2, mv.w * 1.4426950408889634f);
                         }
+                        if (j + 1 < nt) stage_mask(j + 1);
                     } else {
 #pragma unroll
                         for (int c = 0; c < 64; ++c) {
@@ -798,6 +846,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row < n)  // lse: [B][H][N], or [H][total] for a packed batch
                 p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
                     (l > 0.0f) ? (m_ref + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
+        }
+        if constexpr (HAS_MASK) {  // a mask copy still in flight (after a timeout) lands before the CTA exits
+            if (mpending) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(smem_u32(mask_bars() + warp), mcount & 1u) &&
+                       global_timer_ns() - t0 < p.timeout_ns) {
+                }
+            }
         }
     }
 

@@ -39,7 +39,7 @@ bool encode_tokens_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_byt
 
 template <typename T, int D, bool CAUSAL, bool MASK>
 int launch_variant(const LaunchArgs &a) {
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, MASK>;
     auto kern = fa_fwd_kernel<T, D, CAUSAL, MASK>;
     // The register split between warpgroups assumes 128 registers per thread at
     // launch (512 x 128 = 256 x 200 + 256 x 56). Refuse to launch otherwise.
@@ -54,6 +54,11 @@ int launch_variant(const LaunchArgs &a) {
     const int BHkv = a.B * a.Hkv;
     if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, BHkv, kBK)) return -5;
     if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, BHkv, kBK)) return -5;
+    // the mask [B][N][N] fp32 as (key, query row, b) with 32-key x 32-row boxes; its row stride must be a
+    // multiple of 16 bytes (N % 4 == 0), otherwise the softmax warps read it directly
+    CUtensorMap tm = tq;
+    const bool mask_tma = MASK && a.mask && (a.N % 4) == 0;
+    if (mask_tma && !encode_rows_map(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.mask, a.N, a.N, a.B, 32)) return -5;
     FwdParams p;
     p.out = a.out;
     p.lse = a.lse;
@@ -71,8 +76,9 @@ int launch_variant(const LaunchArgs &a) {
     p.cu_seqlens = nullptr;
     p.total = 0;
     p.Hkv = a.Hkv;
+    p.mask_tma = mask_tma ? 1 : 0;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tm, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
@@ -106,8 +112,9 @@ int launch_varlen_variant(const LaunchArgs &a) {
     p.cu_seqlens = a.cu_seqlens;
     p.total = a.total;
     p.Hkv = a.Hkv;
+    p.mask_tma = 0;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tq, p);  // no mask: tq stands in for its map
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

@@ -1,8 +1,10 @@
-// warp_mma.cuh -- warp-level 16x8x16 MMA, ldmatrix and cp.async wrappers for the
+// warp_mma.cuh -- warp-level 16x8x16 MMA and ldmatrix wrappers for the
 // small-tile (decoding) kernels: one-instruction inline-PTX wrappers written
 // from the PTX ISA description of each instruction.
 #pragma once
 #include <stdint.h>
+
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -43,15 +45,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "memory");
 }
 
-// 16-byte asynchronous global -> shared copy; with src_bytes = 0 nothing is read
-// and the 16 bytes are zero-filled.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// cp_async16, cp_async_commit and cp_async_wait live in ptx.cuh.
 
 }  // namespace fa

@@ -53,6 +53,8 @@ SMALL = [
     (2, 2, 300, 128, "fp16", False, True),
     (1, 3, 513, 128, "bf16", True, True),
     (2, 2, 260, 64, "fp16", True, True),
+    (1, 2, 20, 128, "bf16", False, True),   # mask by TMA: every box reaches past N (zero fill)
+    (2, 1, 68, 64, "bf16", True, True),     # mask by TMA: second key block ragged, rows past N in the tile
     (1, 1, 256, 64, "fp32", False, False),
     (1, 2, 300, 64, "fp32", True, False),
     (1, 2, 200, 64, "fp32", False, True),
