@@ -119,7 +119,8 @@ struct FwdParams {
     int *status;        // device status word
     int B, H, N;
     int kv_group;       // query heads per key/value head (1 unless grouped-query attention)
-    int n_items;        // B * H * ceil(N / 256)
+    int n_items;        // work units: n_pair two-tile items, then single query tiles
+    int n_pair;         // two-tile items (B * H * ceil(N / 256) unless the tail is split, see split_tail)
     int n_qblk;         // ceil(N / 256)
     int n_kv;           // ceil(N / 64)
     float scale_log2;   // scale * log2(e)
@@ -156,13 +157,22 @@ __device__ __forceinline__ void item_coords(const FwdParams &p, int item, int &b
 // token index of the sequence's first row.
 struct Item {
     int bh, q0, n, tok0;
+    int nrow;  // rows of the sequence this unit covers end before nrow (q0 + 128 for a single-tile unit)
 };
 
 __device__ __forceinline__ Item get_item(const FwdParams &p, int item) {
     Item it;
+    // units past n_pair are the two query tiles of the remaining items, one at a time
+    const int split = item - p.n_pair;
+    if (split >= 0) item = p.n_pair + (split >> 1);
     item_coords(p, item, it.bh, it.q0);
     it.n = p.N;
     it.tok0 = 0;
+    it.nrow = p.N;
+    if (split >= 0) {
+        it.q0 += (split & 1) * kBQ;
+        it.nrow = min(p.N, it.q0 + kBQ);
+    }
     return it;
 }
 
@@ -250,6 +260,7 @@ struct VarlenCursor {
                 it.q0 = thr;
                 it.n = __shfl_sync(0xffffffffu, n, src);
                 it.tok0 = __shfl_sync(0xffffffffu, a, src);
+                it.nrow = it.n;
                 return true;
             }
             rank += nb;
@@ -263,7 +274,7 @@ struct VarlenCursor {
 template <bool CAUSAL>
 __device__ __forceinline__ int tile_nkv(const Item &it, int t) {
     const int r0 = it.q0 + t * kBQ;
-    if (r0 >= it.n) return 0;
+    if (r0 >= it.nrow) return 0;
     if (!CAUSAL) return (it.n + kBK - 1) / kBK;
     const int last_row = min(it.n, r0 + kBQ) - 1;
     return last_row / kBK + 1;
@@ -379,6 +390,7 @@ struct ItemIter<true> {
         it.q0 = d.y;
         it.n = d.z;
         it.tok0 = d.w;
+        it.nrow = d.z;
         return true;
     }
 };

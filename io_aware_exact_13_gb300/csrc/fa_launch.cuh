@@ -37,6 +37,18 @@ bool encode_rows_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes
 bool encode_tokens_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *base, int d,
                        int heads, int total, int box_rows);
 
+// Work units of the dense schedule. n2 two-tile items over G persistent CTAs leave a last wave of
+// rem = n2 % G items (all n2 when n2 < G). When those rem items, cut into their 2 rem single query tiles, fit
+// in one wave, they are cut: the last wave then takes about the time of one tile instead of two. Equal
+// (non-causal) items gain whenever that holds; causal items are sorted longest first, so only a grid with
+// at most G / 2 items (one wave with idle CTAs) gains.
+inline void split_tail(FwdParams &p, int n2, int G, bool causal) {
+    const int rem = n2 % G;
+    const bool split = rem > 0 && 2 * rem <= G && (!causal || n2 <= G / 2);
+    p.n_pair = split ? n2 - rem : n2;
+    p.n_items = split ? n2 + rem : n2;
+}
+
 template <typename T, int D, bool CAUSAL, bool MASK>
 int launch_variant(const LaunchArgs &a) {
     using C = Cfg<T, D, MASK>;
@@ -70,7 +82,7 @@ int launch_variant(const LaunchArgs &a) {
     p.N = a.N;
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
     p.n_kv = (a.N + kBK - 1) / kBK;
-    p.n_items = BH * p.n_qblk;
+    split_tail(p, BH * p.n_qblk, a.num_sms, CAUSAL);
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
     p.cu_seqlens = nullptr;
@@ -107,6 +119,7 @@ int launch_varlen_variant(const LaunchArgs &a) {
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
     p.n_kv = (a.N + kBK - 1) / kBK;
     p.n_items = a.B * a.H * p.n_qblk;
+    p.n_pair = p.n_items;  // the packed-batch list has its own order
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
     p.cu_seqlens = a.cu_seqlens;

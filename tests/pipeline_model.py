@@ -107,9 +107,15 @@ def simulate(N, causal, items, ring, seed, softmax_warps=4, per_buffer_p=True, r
         return (f"p_full{t}{g & 1}", g >> 1) if per_buffer_p else (f"p_full{t}", g)
 
     def counts(q0):
-        # an item is a first query row, or (first row, sequence length) in a packed batch
-        q0, n_seq = (q0, N) if isinstance(q0, int) else q0
-        n = [tile_nkv(n_seq, causal, q0, t) for t in range(2)]
+        # an item is a first query row, or (first row, sequence length) in a packed batch, or
+        # (first row, sequence length, row limit) for a single-tile unit of the dense schedule
+        if isinstance(q0, int):
+            q0, n_seq, nrow = q0, N, N
+        elif len(q0) == 2:
+            (q0, n_seq), nrow = q0, q0[1]
+        else:
+            q0, n_seq, nrow = q0
+        n = [tile_nkv(n_seq, causal, q0, t) if q0 + t * BQ < nrow else 0 for t in range(2)]
         return n, max(n)
 
     def producer():

@@ -50,6 +50,7 @@ SMALL = [
     (2, 3, 384, 128, "bf16", True, False),
     (1, 2, 1000, 128, "bf16", True, False),
     (1, 2, 1000, 64, "bf16", False, False),
+    (1, 63, 1024, 64, "bf16", False, False),  # 252 two-tile items: last wave too full to cut into single tiles
     (2, 2, 300, 128, "fp16", False, True),
     (1, 3, 513, 128, "bf16", True, True),
     (2, 2, 260, 64, "fp16", True, True),

@@ -101,3 +101,17 @@ def test_item_ring_without_empty_wait_is_caught():
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("ring", [2, 5])
+def test_single_tile_units(causal, ring):
+    """The dense schedule may cut its last items into single query tiles (tile 1 of
+    the unit has no rows while tile 0 sees every key block): two-tile items
+    followed by such units complete without aliasing."""
+    N = 1000
+    pairs = [qb * ROWS for qb in range(3, -1, -1)]
+    units = [(q0, N, min(N, q0 + 128)) for qb in range(3, -1, -1) for q0 in (qb * ROWS, qb * ROWS + 128)]
+    for seed in range(8):
+        assert simulate(N, causal, pairs[:2] + units[4:], ring, seed)
+        assert simulate(N, causal, units, ring, seed)
