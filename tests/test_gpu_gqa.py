@@ -44,6 +44,25 @@ def test_gqa_matches_repeated_heads(fa, B, H, Hkv, N, d, dtype, causal):
     compare(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("N,causal", [(300, False), (260, True), (517, False)])
+def test_gqa_with_additive_mask(fa, N, causal):
+    """Grouped-query attention with an additive [B,N,N] mask (shared by all heads of a batch index;
+    N % 4 == 0 takes the TMA mask copies, 517 the direct loads)."""
+    B, H, Hkv, d = 2, 6, 2, 128
+    q, _, _, mask = make_qkv(B, H, N, d, "bf16", seed=N + 5, mask_frac=0.2, full_row_frac=0.02)
+    _, k, v, _ = make_qkv(B, Hkv, N, d, "bf16", seed=N + 6)
+    dev = torch.device("cuda")
+    out = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    fa.fa_fwd_gqa(q.to(dev), k.to(dev), v.to(dev), mask.to(dev), out, lse, 1 / math.sqrt(d), causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    g = H // Hkv
+    ref_o, ref_l = oracle.attention(q, k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1), mask=mask,
+                                    scale=1 / math.sqrt(d), causal=causal)
+    compare(out, lse, ref_o, ref_l)
+
+
 def test_gqa_workload_every_head(fa):
     """The benchmark's grouped-query workload in the benchmark's launch; every
     query head against the oracle with its K/V head repeated."""
