@@ -190,7 +190,7 @@ int fa_fwd_varlen_fp16(const void *q, const void *k, const void *v, void *out, f
  * workspace: caller-owned device memory, 256-byte aligned, of at least
  * fa_bwd_workspace_bytes(B, H, N, d) bytes (an fp32 dQ accumulator of
  * B*H*N*d floats plus two per-row fp32 arrays); contents on entry do not
- * matter. Calls sharing a workspace must not overlap on the GPU. Four kernels
+ * matter. Calls sharing a workspace must not overlap on the GPU. Three kernels
  * are enqueued on `stream`: row statistics, the tiled backward, and the
  * conversion of the dQ accumulator. d in {64, 128}.
  * Errors as for fa_fwd; FA_ERR_WORKSPACE if the workspace is missing, too

@@ -24,6 +24,28 @@ int launch_fwd_varlen_bf16(const LaunchArgs &a);
 int launch_fwd_varlen_fp16(const LaunchArgs &a);
 }  // namespace fa
 
+namespace fa {
+// FA_LOG=1 in the environment prints one line per call to stderr: the entry
+// point, the kernel variant it dispatches to and the problem size.
+static bool log_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("FA_LOG");
+        return v != nullptr && v[0] != '\0' && v[0] != '0';
+    }();
+    return on;
+}
+void log_call(const char *fmt, ...) {
+    if (!log_enabled()) return;
+    va_list ap;
+    va_start(ap, fmt);
+    std::fputs("[fa] ", stderr);
+    std::vfprintf(stderr, fmt, ap);
+    std::fputc('\n', stderr);
+    va_end(ap);
+}
+}  // namespace fa
+using fa::log_call;
+
 // Device status word: FA_OK, or FA_ERR_TIMEOUT once any bounded wait gave up.
 __device__ int g_fa_status = 0;
 
@@ -78,24 +100,6 @@ DeviceInfo *device_info() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// FA_LOG=1 in the environment prints one line per call to stderr: the entry
-// point, the kernel variant it dispatches to and the problem size.
-bool log_enabled() {
-    static const bool on = [] {
-        const char *v = std::getenv("FA_LOG");
-        return v != nullptr && v[0] != '\0' && v[0] != '0';
-    }();
-    return on;
-}
-void log_call(const char *fmt, ...) {
-    if (!log_enabled()) return;
-    va_list ap;
-    va_start(ap, fmt);
-    std::fputs("[fa] ", stderr);
-    std::vfprintf(stderr, fmt, ap);
-    std::fputc('\n', stderr);
-    va_end(ap);
-}
 
 enum class Type { BF16, FP16, FP32 };
 

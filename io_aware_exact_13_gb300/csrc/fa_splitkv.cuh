@@ -31,5 +31,7 @@ int launch_splitkv(const SplitKVArgs &a, bool fp16);
 
 // Resident CTAs per SM of the partial kernel used for (d, Nq) (bf16 variant).
 int splitkv_blocks_per_sm(int d, int Nq);
+// FA_LOG=1: one line per call to stderr (defined in fa_api.cu).
+void log_call(const char *fmt, ...);
 
 }  // namespace fa

@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -32,27 +33,27 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_splitkv_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevicesNA = 64;
-struct ScratchSlot {
-    std::once_flag once;
-    void *ptr = nullptr;  // device address of g_splitkv_scratch on this device
-    bool ok = false;
-};
-ScratchSlot g_scratch[kMaxDevicesNA];
+std::mutex g_scratch_mutex;
+std::atomic<void *> g_scratch[kMaxDevicesNA];  // device address of g_splitkv_scratch per device, or null
 
-// Set-up, once per device, with that device current (it is the caller's
-// current device when the first call is made on it).
+// Set-up per device, with that device current (it is the caller's current
+// device when a call is made on it). Only a successful lookup is kept: if the
+// lookup fails (for instance because the first call was made while a stream
+// capture was in progress), the next call tries again.
 void *scratch_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesNA) return nullptr;
-    ScratchSlot &s = g_scratch[dev];
-    std::call_once(s.once, [&s] {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) == cudaSuccess && ptr != nullptr) {
-            s.ptr = ptr;
-            s.ok = true;
-        }
-    });
-    return s.ok ? s.ptr : nullptr;
+    void *ptr = g_scratch[dev].load(std::memory_order_acquire);
+    if (ptr) return ptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    ptr = g_scratch[dev].load(std::memory_order_relaxed);
+    if (ptr) return ptr;
+    if (cudaGetSymbolAddress(&ptr, g_splitkv_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();  // leave no sticky error from the failed lookup behind
+        return nullptr;
+    }
+    g_scratch[dev].store(ptr, std::memory_order_release);
+    return ptr;
 }
 
 bool aligned_na(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -72,6 +73,8 @@ extern "C" int fa_fwd_splitkv_noalloc(const void *q, const void *k, const void *
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const int64_t rows = static_cast<int64_t>(B) * H * Nq;
     if (fa::splitkv_workspace_bytes(rows, d, n_splits) > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
+    fa::log_call("split-KV noalloc bf16 d=%d causal=%d B=%d H=%d Nq=%d Nk=%d splits=%d", d, causal ? 1 : 0, B, H,
+                 Nq, Nk, n_splits);
     void *scratch = scratch_address();
     if (!scratch) return FA_ERR_LAUNCH;
     fa::SplitKVArgs a;

@@ -143,6 +143,25 @@ def test_bwd_full_size_every_head(fa, name):
     _cmp("dv", dv, rv)
 
 
+def test_bwd_full_size_d128_every_head(fa):
+    """The d = 128 backward at its benchmark size (B1 H32 N8192 causal), in the
+    benchmark's launch; dQ, dK, dV of all 32 heads against the oracle's
+    gradients (the fp64 backward over all heads takes about a minute of host
+    time)."""
+    w = BWD_WORKLOADS["bwd_b1h32_n8192_d128_bf16_causal"]
+    q, k, v, do = make_bwd(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed)
+    dev = torch.device("cuda")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), scale=w.scale, causal=w.causal)
+    dq, dk, dv = fa.attention_backward(q.to(dev), k.to(dev), v.to(dev), o, do.to(dev), lse, scale=w.scale,
+                                       causal=w.causal)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, scale=w.scale, causal=w.causal)
+    _cmp("dq", dq, rq)
+    _cmp("dk", dk, rk)
+    _cmp("dv", dv, rv)
+
+
 def test_bwd_host_validation(fa):
     dev = torch.device("cuda")
     q = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device=dev)

@@ -59,6 +59,10 @@ SMALL = [
     (1, 1, 256, 64, "fp32", False, False),
     (1, 2, 300, 64, "fp32", True, False),
     (1, 2, 200, 64, "fp32", False, True),
+    (1, 2, 300, 128, "fp32", True, False),   # d = 128 on the fp32 path: causal, ragged tail
+    (2, 1, 200, 128, "fp32", False, True),   # masked, rows fully masked
+    (1, 2, 129, 128, "fp32", True, True),    # causal and masked together, one row past a block
+    (1, 1, 1, 128, "fp32", False, False),    # a single row and key
 ]
 
 
