@@ -709,7 +709,7 @@ def main():
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--timed-s", type=float, default=1.0,
+    ap.add_argument("--timed-s", type=float, default=2.0,
                     help="repeat the K-step timed region until about this many seconds are covered")
     ap.add_argument("--max-repeats", type=int, default=200)
     ap.add_argument("--no-materialised", action="store_true",

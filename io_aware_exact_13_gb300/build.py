@@ -66,7 +66,7 @@ def check_ptxas_log(log: str) -> tuple[list[str], list[str]]:
         if m and kernel and (int(m.group(1)) or int(m.group(2))):
             warnings.append(f"{kernel}: spills ({m.group(0)})")
         m = re.search(r"Used (\d+) registers", line)
-        if m and kernel and "fa_fwd_kernel" in kernel and int(m.group(1)) != 128:
+        if m and kernel and re.search(r"fa_fwd_(bk128_)?kernel", kernel) and int(m.group(1)) != 128:
             problems.append(f"{kernel}: uses {m.group(1)} registers, expected 128")
     return problems, warnings
 

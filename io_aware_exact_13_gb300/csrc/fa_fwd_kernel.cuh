@@ -270,14 +270,14 @@ struct VarlenCursor {
     }
 };
 
-// Number of K/V blocks query tile t of an item must visit.
-template <bool CAUSAL>
+// Number of BK-key blocks query tile t of an item must visit.
+template <bool CAUSAL, int BK = kBK>
 __device__ __forceinline__ int tile_nkv(const Item &it, int t) {
     const int r0 = it.q0 + t * kBQ;
     if (r0 >= it.nrow) return 0;
-    if (!CAUSAL) return (it.n + kBK - 1) / kBK;
+    if (!CAUSAL) return (it.n + BK - 1) / BK;
     const int last_row = min(it.n, r0 + kBQ) - 1;
-    return last_row / kBK + 1;
+    return last_row / BK + 1;
 }
 
 template <int R>

@@ -1,10 +1,11 @@
-// bf16 instantiations of the forward kernel for packed variable-length batches.
+// bf16 instantiations of the forward for packed variable-length batches
+// (the 128-key-block kernel).
 #include "fa_launch.cuh"
 
 namespace fa {
 int launch_fwd_varlen_bf16(const LaunchArgs &a) {
-    if (a.d == 128) return launch_varlen_d<__nv_bfloat16, 128>(a);
-    if (a.d == 64) return launch_varlen_d<__nv_bfloat16, 64>(a);
+    if (a.d == 128) return launch_bk128_d<__nv_bfloat16, 128, true>(a);
+    if (a.d == 64) return launch_bk128_d<__nv_bfloat16, 64, true>(a);
     return -4;
 }
 }  // namespace fa

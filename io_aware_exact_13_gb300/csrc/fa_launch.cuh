@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_fwd_bk128.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -94,19 +95,28 @@ int launch_variant(const LaunchArgs &a) {
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
-template <typename T, int D, bool CAUSAL>
-int launch_varlen_variant(const LaunchArgs &a) {
-    using C = Cfg<T, D>;
-    auto kern = fa_fwd_kernel<T, D, CAUSAL, false, true>;
+// The 128-key-block kernel (no mask): dense [B][H][N][d] tensors, or a packed batch.
+template <typename T, int D, bool CAUSAL, bool VARLEN>
+int launch_bk128(const LaunchArgs &a) {
+    using C = Cfg128<T, D>;
+    auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN>;
+    // The register split between warpgroups assumes 128 registers per thread at
+    // launch (512 x 128 = 256 x 192 + 256 x 64). Refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
-    if (attr.numRegs * kThreads < 256 * 200 + 256 * 56) return -5;
+    if (attr.numRegs * kThreads < 256 * 192 + 256 * 64) return -5;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return -5;
     CUtensorMap tq, tk, tv;
-    if (!encode_tokens_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.H, a.total, kBQ)) return -5;
-    if (!encode_tokens_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.Hkv, a.total, kBK)) return -5;
-    if (!encode_tokens_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.Hkv, a.total, kBK)) return -5;
+    if (VARLEN) {
+        if (!encode_tokens_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.H, a.total, kBQ)) return -5;
+        if (!encode_tokens_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.Hkv, a.total, kBK128)) return -5;
+        if (!encode_tokens_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.Hkv, a.total, kBK128)) return -5;
+    } else {
+        if (!encode_rows_map(&tq, Elem<T>::tma, sizeof(T), a.q, D, a.N, a.B * a.H, kBQ)) return -5;
+        if (!encode_rows_map(&tk, Elem<T>::tma, sizeof(T), a.k, D, a.N, a.B * a.Hkv, kBK128)) return -5;
+        if (!encode_rows_map(&tv, Elem<T>::tma, sizeof(T), a.v, D, a.N, a.B * a.Hkv, kBK128)) return -5;
+    }
     FwdParams p;
     p.out = a.out;
     p.lse = a.lse;
@@ -115,31 +125,35 @@ int launch_varlen_variant(const LaunchArgs &a) {
     p.B = a.B;
     p.H = a.H;
     p.kv_group = a.H / a.Hkv;
-    p.N = a.N;  // max_seqlen
+    p.N = a.N;  // max_seqlen for a packed batch
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
-    p.n_kv = (a.N + kBK - 1) / kBK;
-    p.n_items = a.B * a.H * p.n_qblk;
-    p.n_pair = p.n_items;  // the packed-batch list has its own order
+    p.n_kv = (a.N + kBK128 - 1) / kBK128;
+    if (VARLEN) {
+        p.n_items = a.B * a.H * p.n_qblk;
+        p.n_pair = p.n_items;  // the packed-batch list has its own order
+    } else {
+        split_tail(p, a.B * a.H * p.n_qblk, a.num_sms, CAUSAL);
+    }
     p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     p.timeout_ns = a.timeout_ns;
-    p.cu_seqlens = a.cu_seqlens;
-    p.total = a.total;
+    p.cu_seqlens = VARLEN ? a.cu_seqlens : nullptr;
+    p.total = VARLEN ? a.total : 0;
     p.Hkv = a.Hkv;
     p.mask_tma = 0;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tq, p);  // no mask: tq stands in for its map
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
-template <typename T, int D>
-int launch_varlen_d(const LaunchArgs &a) {
-    return a.causal ? launch_varlen_variant<T, D, true>(a) : launch_varlen_variant<T, D, false>(a);
+template <typename T, int D, bool VARLEN>
+int launch_bk128_d(const LaunchArgs &a) {
+    return a.causal ? launch_bk128<T, D, true, VARLEN>(a) : launch_bk128<T, D, false, VARLEN>(a);
 }
 
+// The 64-key-block kernel with an additive mask.
 template <typename T, int D>
-int launch_d(const LaunchArgs &a) {
-    if (a.causal) return a.mask ? launch_variant<T, D, true, true>(a) : launch_variant<T, D, true, false>(a);
-    return a.mask ? launch_variant<T, D, false, true>(a) : launch_variant<T, D, false, false>(a);
+int launch_masked_d(const LaunchArgs &a) {
+    return a.causal ? launch_variant<T, D, true, true>(a) : launch_variant<T, D, false, true>(a);
 }
 
 }  // namespace fa

@@ -407,3 +407,238 @@ def simulate_bwd_halves(n_it, stages, seed):
             del agents[c]
             waiting[c] = None
     return True
+
+
+def simulate_bk128(N, causal, items, rk, rv, seed, alias, softmax_warps=4, rescale_prob=0.1, item_ring=0,
+                   in_order_pv_then_s=True, pv_wait_every_block=True):
+    """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
+    one issuing warp per query tile (S_t and P_t V products), the softmax warps of
+    both tiles, and (``item_ring`` > 0) the packed-batch item list.
+
+    ``alias`` is the d = 128 layout, where P_t is written over S_t's tensor-memory
+    columns: the issuer orders O += P V(j) before S(j+1). Besides the barrier
+    checks of ``simulate`` this model tracks what each tile's S/P columns and P
+    buffer hold, so that a product that overwrites P before the P V product has
+    read it, or a softmax that reads S before it is complete, fails here.
+    ``in_order_pv_then_s=False`` is an aliasing issuer that issues S(j+1) before
+    P V(j) (it must be caught); ``pv_wait_every_block=False`` is a softmax that
+    skips its per-block wait for the previous P V commit (the epilogue's parity
+    wait then can alias, which must be caught too)."""
+    rnd = random.Random(seed)
+    B = {}
+    BK128 = 128
+
+    def bar(name, count):
+        B[name] = Bar(name, count)
+
+    for t in range(2):
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", BQ), ("p_full", BQ),
+                        ("pv_done", 1)):
+            bar(f"{name}{t}", c)
+    for s in range(rk):
+        bar(f"k_full{s}", 1)
+        bar(f"k_empty{s}", 2)
+    for s in range(rv):
+        bar(f"v_full{s}", 1)
+        bar(f"v_empty{s}", 2)
+    consumers = 3 + 2 * softmax_warps
+    for s in range(item_ring):
+        bar(f"item_full{s}", 1)
+        bar(f"item_empty{s}", consumers)
+    tensor_pipe, tma = [], []
+    # tensor-memory contents per tile: the S columns ("S", j) / ("P", j) and, without aliasing, the P buffer
+    # (per softmax warp: each warp owns 32 of the 128 lanes; a product writes or reads all of them)
+    scols = [[None] * softmax_warps for _ in range(2)]
+    pbuf = [[None] * softmax_warps for _ in range(2)]
+    sread = [set(), set()]      # S blocks the softmax has finished copying out (all its warps)
+    sreaders = [{}, {}]
+    pv_read = [set(), set()]    # P blocks whose P V product has executed
+    o_last = [None, None]       # the last P V product that wrote O_t
+
+    def nkv(n_seq, q0, t):
+        r0 = q0 + t * BQ
+        if r0 >= n_seq:
+            return 0
+        if not causal:
+            return (n_seq + BK128 - 1) // BK128
+        return (min(n_seq, r0 + BQ) - 1) // BK128 + 1
+
+    def counts(q0):
+        if isinstance(q0, int):
+            q0, n_seq, nrow = q0, N, N
+        elif len(q0) == 2:
+            (q0, n_seq), nrow = q0, q0[1]
+        else:
+            q0, n_seq, nrow = q0
+        n = [nkv(n_seq, q0, t) if q0 + t * BQ < nrow else 0 for t in range(2)]
+        return n, max(n)
+
+    def take(i):
+        if item_ring:
+            yield ("wait", f"item_full{i % item_ring}", i // item_ring)
+            yield ("arrive", f"item_empty{i % item_ring}", 1)
+
+    def scheduler():
+        for i in range(len(items) + 1):
+            yield ("wait", f"item_empty{i % item_ring}", i // item_ring - 1)
+            yield ("arrive", f"item_full{i % item_ring}", 1)
+
+    def producer():
+        qcount, kpos, vpos = [0, 0], 0, 0
+        for i, q0 in enumerate(items):
+            yield from take(i)
+            n, nmax = counts(q0)
+            for t in range(2):
+                if n[t]:
+                    yield ("wait", f"q_empty{t}", qcount[t] - 1)
+                    tma.append(f"q_full{t}")
+                    qcount[t] += 1
+            order = (["K"] if nmax > 0 else []) + [x for j in range(nmax)
+                                                   for x in (["K"] if j + 1 < nmax else []) + ["V"]]
+            for kind in order:
+                if kind == "K":
+                    yield ("wait", f"k_empty{kpos % rk}", kpos // rk - 1)
+                    tma.append(f"k_full{kpos % rk}")
+                    kpos += 1
+                else:
+                    yield ("wait", f"v_empty{vpos % rv}", vpos // rv - 1)
+                    tma.append(f"v_full{vpos % rv}")
+                    vpos += 1
+        yield from take(len(items))
+
+    def issuer(t):
+        st = {"q": 0, "k": 0, "v": 0, "p": 0, "s": 0}
+
+        def issue_s(j, nt, gidx):
+            s = st["k"] % rk
+            yield ("wait", f"k_full{s}", st["k"] // rk)
+            st["k"] += 1
+            if j >= nt:
+                yield ("arrive", f"k_empty{s}", 1)
+                return
+            if not alias and st["s"] > 0:
+                yield ("wait", f"s_free{t}", st["s"] - 1)
+            st["s"] += 1
+            tensor_pipe.extend([("mma", "S", t, gidx), ("commit", f"s_full{t}")]
+                               + ([("commit", f"q_empty{t}")] if j == nt - 1 else []) + [("commit", f"k_empty{s}")])
+
+        def issue_pv(j, nt, gidx):
+            s = st["v"] % rv
+            yield ("wait", f"v_full{s}", st["v"] // rv)
+            st["v"] += 1
+            if j >= nt:
+                yield ("arrive", f"v_empty{s}", 1)
+                return
+            yield ("wait", f"p_full{t}", st["p"])
+            st["p"] += 1
+            tensor_pipe.extend([("mma", "PV", t, gidx), ("commit", f"pv_done{t}"), ("commit", f"v_empty{s}")])
+
+        g0 = 0  # index of the tile's first block of the item among all its blocks
+        for i, q0 in enumerate(items):
+            yield from take(i)
+            n, nmax = counts(q0)
+            nt = n[t]
+            if nmax == 0:
+                continue
+            if nt:
+                yield ("wait", f"q_full{t}", st["q"])
+                st["q"] += 1
+            yield from issue_s(0, nt, g0)
+            for j in range(nmax):
+                if alias and in_order_pv_then_s:
+                    yield from issue_pv(j, nt, g0 + j)
+                    if j + 1 < nmax:
+                        yield from issue_s(j + 1, nt, g0 + j + 1)
+                else:
+                    if j + 1 < nmax:
+                        yield from issue_s(j + 1, nt, g0 + j + 1)
+                    yield from issue_pv(j, nt, g0 + j)
+            g0 += nt
+        yield from take(len(items))
+
+    def softmax(t, w):
+        scount = g = 0
+        for i, q0 in enumerate(items):
+            yield from take(i)
+            n, _ = counts(q0)
+            nt = n[t]
+            if not nt:
+                continue
+            for j in range(nt):
+                yield ("wait", f"s_full{t}", scount)
+                scount += 1
+                assert scols[t][w] == ("S", g), f"tile {t}: softmax reads S({g}) but the columns hold {scols[t][w]}"
+                sreaders[t][g] = sreaders[t].get(g, 0) + 1
+                if sreaders[t][g] == softmax_warps:
+                    sread[t].add(g)
+                if not alias:
+                    yield ("arrive", f"s_free{t}", BQ // softmax_warps)
+                if j > 0 and (pv_wait_every_block or rnd.random() < rescale_prob):
+                    yield ("wait", f"pv_done{t}", g - 1)
+                # store P(g)
+                if alias:
+                    assert scols[t][w] == ("S", g), f"tile {t}: P({g}) written over {scols[t][w]}"
+                    scols[t][w] = ("P", g)
+                else:
+                    assert pbuf[t][w] is None or pbuf[t][w][1] in pv_read[t], (
+                        f"tile {t}: P({g}) overwrites P{pbuf[t][w]} before its P V product read it")
+                    pbuf[t][w] = ("P", g)
+                yield ("arrive", f"p_full{t}", BQ // softmax_warps)
+                g += 1
+            yield ("wait", f"pv_done{t}", g - 1)  # epilogue
+            assert o_last[t] == g - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]}) of the next item"
+        yield from take(len(items))
+
+    def execute(kind, t, g):
+        if kind == "S":
+            for prev in scols[t]:
+                if alias:  # the columns must hold a P whose P V product has read it
+                    assert prev is None or (prev[0] == "P" and prev[1] in pv_read[t]), (
+                        f"tile {t}: S({g}) overwrites {prev} before it was consumed")
+                else:
+                    assert prev is None or prev[1] in sread[t], f"tile {t}: S({g}) overwrites S{prev} before it was read"
+            scols[t] = [("S", g)] * softmax_warps
+        else:
+            for held in (scols[t] if alias else pbuf[t]):
+                assert held == ("P", g), f"tile {t}: P V({g}) reads {held}"
+            pv_read[t].add(g)
+            o_last[t] = g
+
+    agents = {"producer": producer(), "I0": issuer(0), "I1": issuer(1)}
+    if item_ring:
+        agents["scheduler"] = scheduler()
+    for t in range(2):
+        for w in range(softmax_warps):
+            agents[f"softmax{t}.{w}"] = softmax(t, w)
+    waiting = {k: None for k in agents}
+    while agents or tensor_pipe or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        if tensor_pipe:
+            ready.append("#tensor")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c == "#tensor":
+            op = tensor_pipe.pop(0)
+            if op[0] == "mma":
+                execute(op[1], op[2], op[3])
+            else:
+                B[op[1]].arrive(1)
+            continue
+        if c == "#tma":
+            B[tma.pop(rnd.randrange(len(tma)))].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

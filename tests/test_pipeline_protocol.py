@@ -115,3 +115,65 @@ def test_single_tile_units(causal, ring):
     for seed in range(8):
         assert simulate(N, causal, pairs[:2] + units[4:], ring, seed)
         assert simulate(N, causal, units, ring, seed)
+
+
+# ---------------------------------------------------------------- the 128-key-block kernel
+def _items128(N, all_blocks):
+    nqb = (N + ROWS - 1) // ROWS
+    return [qb * ROWS for qb in range(nqb - 1, -1, -1)] if all_blocks else [(nqb - 1) * ROWS]
+
+
+@pytest.mark.parametrize("N,causal", [(1000, True), (4096, True), (384, True), (200, True), (129, False),
+                                      (1000, False), (64, False), (1, True), (256, True), (257, False)])
+@pytest.mark.parametrize("alias,rk,rv", [(True, 3, 2), (False, 6, 6), (True, 2, 2)])
+def test_bk128_protocol_completes_without_hazards(N, causal, alias, rk, rv):
+    from pipeline_model import simulate_bk128
+
+    for all_blocks in (False, True):
+        for seed in range(4 if N <= 1000 else 2):
+            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, alias)
+
+
+def test_bk128_single_tile_units_and_packed_items():
+    """Single-tile units of the dense schedule and packed-batch items (some with no rows),
+    taken from the item ring as the packed kernel does."""
+    from pipeline_model import simulate_bk128
+
+    lengths = [0, 1, 127, 128, 129, 255, 256, 257, 700, 0, 300]
+    n_items = (max(lengths) + ROWS - 1) // ROWS
+    packed = [(qb * ROWS, L) for qb in range(n_items - 1, -1, -1) for L in lengths]
+    single = [(512, 1000, 640), (512, 1000, 1000), (768, 1000, 896), (0, 1000, 128)]
+    for alias in (True, False):
+        for seed in range(4):
+            assert simulate_bk128(max(lengths), True, packed, 3, 2, seed, alias, item_ring=4)
+            assert simulate_bk128(max(lengths), False, packed, 6, 6, seed, alias, item_ring=4)
+            assert simulate_bk128(1000, True, single, 3, 2, seed, alias)
+
+
+def test_bk128_overwriting_p_before_its_product_is_caught():
+    """An aliasing issuer that issues S(j+1) before P V(j) overwrites P: caught."""
+    from pipeline_model import simulate_bk128
+
+    caught = 0
+    for seed in range(10):
+        try:
+            simulate_bk128(1000, True, _items128(1000, True), 3, 2, seed, True, in_order_pv_then_s=False)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
+
+
+def test_bk128_skipping_the_per_block_commit_wait_is_caught():
+    """d = 64 (P_t in its own buffer): a softmax that stores P(j) without waiting
+    for the commit of P V(j-1) overwrites a P that the tensor core has not read
+    yet: caught."""
+    from pipeline_model import simulate_bk128
+
+    caught = 0
+    for seed in range(20):
+        try:
+            simulate_bk128(2048, False, _items128(2048, True), 6, 6, seed, False, pv_wait_every_block=False,
+                           rescale_prob=0.0)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
