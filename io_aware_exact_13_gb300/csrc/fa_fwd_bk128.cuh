@@ -26,13 +26,26 @@
 //            as soon as the softmax has copied S_t(j) to registers, so the
 //            softmax of block j+1 can start while P_t V_j runs.
 //
+// Softmax: both warpgroups work on one tile at a time. Warpgroup h takes keys
+// [64 h, 64 h + 64) of each 128-key block; thread r of each owns query row r
+// (TMEM lane r). The two halves of a row agree on the row maximum through
+// shared memory (warps q and q + 4 own the same 32 lanes and meet at a named
+// barrier), so both keep the same reference maximum; each keeps its own partial
+// denominator, and the two are added at the epilogue. The warpgroups take the
+// two tiles in turn: while they compute one tile's P, the tensor core runs the
+// other tile's P V and next S. (One warpgroup per tile, each thread doing all
+// 128 keys of its row, ran the two tiles' softmax passes side by side on the
+// same schedulers: about 2200 cycles per block each, twice the tile's tensor
+// time.)
+//
 // Roles (16 warps, one persistent CTA per SM):
-//   warps 0-3   softmax + epilogue for query tile 0 (thread r = row r = TMEM lane r)
-//   warps 4-7   softmax + epilogue for query tile 1
+//   warps 0-7   softmax + epilogue: warpgroup h = warp / 4 takes key half h
 //   warp  8     TMA producer: Q tiles per item, then K and V rings
 //   warps 9-10  issuer of tile t = warp - 9: S_t products and P_t V products
 //   warp  11    packed batch only: publishes the CTA's work items (ItemRing)
 //   warps 12-15 idle (they complete the last warpgroup)
+// Shared memory holds no static variables: the abort word, the item ring and
+// the row-maximum exchange live after the barriers in the dynamic region.
 #pragma once
 #include "fa_fwd_kernel.cuh"
 
@@ -40,6 +53,7 @@ namespace fa {
 
 constexpr int kBK128 = 128;           // keys per K/V block
 constexpr int kItemConsumers128 = 11; // producer, two issuers, eight softmax warps
+constexpr int kStatusSmemAlign = -5;  // device status: the dynamic shared memory base was misaligned
 
 template <typename T, int D>
 struct Cfg128 {
@@ -73,10 +87,18 @@ struct Cfg128 {
     // q_full[2] q_empty[2] k_full[RK] k_empty[RK] v_full[RV] v_empty[RV] s_full[2] s_free[2] p_full[2]
     // pv_done[2] drain
     static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 8 + 1;
-    static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int SMEM_TMEM_SLOT = SMEM_BAR + ((NUM_BARS * 8 + 15) / 16) * 16;
+    static constexpr int SMEM_XBAR = SMEM_TMEM_SLOT + 16;         // 4 exchange barriers (one per lane quadrant)
+    static constexpr int SMEM_XCH = SMEM_XBAR + 32;               // float [2 parity][2 halves][128 rows]
+    static constexpr int SMEM_RING = SMEM_XCH + 2 * 2 * 128 * 4;  // ItemRing (packed batches)
+    static constexpr int SMEM_ABORT = SMEM_RING + 128;
+    static constexpr int SMEM_USED = SMEM_ABORT + 16;
+    // up to 1024 bytes to align the base (SW128 tiles need 1024-byte alignment), within the 227 KB limit
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024 <= 232448 ? SMEM_USED + 1024 : 232448;
+    static constexpr int SLACK = SMEM_BYTES - SMEM_USED;
     static_assert(NCH >= 1 && ROW_BYTES % 128 == 0, "row must be a whole number of 128-byte swizzle rows");
     static_assert(RK >= 2 && RV >= 2, "K/V rings too small");
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SLACK >= 256, "shared memory budget");
     static_assert(TM_O + 2 * D <= 512 && TM_P + 2 * TM_P_STRIDE <= (ALIAS ? 256 : 512), "tensor memory budget");
 };
 
@@ -101,21 +123,6 @@ struct Sync128 {
     __device__ __forceinline__ uint32_t drain() const { return at(B0 + 8); }
 };
 
-// Row maximum of 128 values: eight independent three-input chains, then a short tree.
-__device__ __forceinline__ float row_max128(const float (&x)[128]) {
-    float m8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
-#pragma unroll
-    for (int c = 24; c < 120; c += 16) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
-    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-}
-
 template <typename T, int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bk128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -123,11 +130,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg128<T, D>;
     constexpr int RK = C::RK, RV = C::RV;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t pad = (uint32_t)((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    if (pad > (uint32_t)C::SLACK) {  // cannot happen with no static shared memory; never overflow
+        if (threadIdx.x == 0) atomicExch(p.status, kStatusSmemAlign);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
     Sync128<RK, RV> sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
-    __shared__ int abort_word;  // static: a constant address, no register holds it
-    volatile int *abort_flag = &abort_word;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_TMEM_SLOT);
+    float *xch = reinterpret_cast<float *>(smem + C::SMEM_XCH);
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + C::SMEM_XBAR);
+    ItemRing *ring = reinterpret_cast<ItemRing *>(smem + C::SMEM_RING);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SMEM_ABORT);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -137,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.q_full(t), 1);
             mbar_init(sy.q_empty(t), 1);
             mbar_init(sy.s_full(t), 1);
-            mbar_init(sy.s_free(t), kBQ);
-            mbar_init(sy.p_full(t), kBQ);
+            mbar_init(sy.s_free(t), 2 * kBQ);  // both softmax warpgroups
+            mbar_init(sy.p_full(t), 2 * kBQ);
             mbar_init(sy.pv_done(t), 1);
         }
         for (int s = 0; s < RK; ++s) {  // a slot is released by both tiles' issuers
@@ -150,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.v_empty(s), 2);
         }
         mbar_init(sy.drain(), 2);  // one commit per issuing warp
+        for (int q = 0; q < 4; ++q) mbar_init(smem_u32(xbar + q), 64);  // warps q and q + 4
         if constexpr (VARLEN) {
-            ItemRing &ring = item_ring();
             for (int i = 0; i < kItemRing; ++i) {
-                mbar_init(smem_u32(&ring.full[i]), 1);
-                mbar_init(smem_u32(&ring.empty[i]), kItemConsumers128);
+                mbar_init(smem_u32(&ring->full[i]), 1);
+                mbar_init(smem_u32(&ring->empty[i]), kItemConsumers128);
             }
         }
         *abort_flag = 0;
@@ -207,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pos;
                 return true;
             };
-            ItemIter<VARLEN> iter(p, abort_flag);
+            ItemIter<VARLEN> iter(p, abort_flag, ring);
             for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int q0 = itm.q0, cur_bh = itm.bh;
                 const int kv_h = (cur_bh % p.H) / p.kv_group;  // grouped-query: kv_group query heads per K/V head
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(sy.v_empty(slot), issue);
                 return true;
             };
-            ItemIter<VARLEN> iter(p, abort_flag);
+            ItemIter<VARLEN> iter(p, abort_flag, ring);
             for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int nt = tile_nkv<CAUSAL, kBK128>(itm, t);
                 const int nmax = max(tile_nkv<CAUSAL, kBK128>(itm, 0), tile_nkv<CAUSAL, kBK128>(itm, 1));
@@ -343,17 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(sy.drain(), issue);
         } else if (VARLEN && warp == 11) {
             // ---------------------------------------------------------- packed-batch item list
-            ItemRing &ring = item_ring();
             VarlenCursor cur(p);
             bool more = true;
             for (uint32_t i = 0; more; ++i) {
                 Item it;
                 more = cur.next(p, it);
                 const uint32_t slot = i % kItemRing;
-                if (!wait_warp(smem_u32(&ring.empty[slot]), ((i / kItemRing) & 1u) ^ 1u, abort_flag, p)) break;
+                if (!wait_warp(smem_u32(&ring->empty[slot]), ((i / kItemRing) & 1u) ^ 1u, abort_flag, p)) break;
                 if (lane == 0) {
-                    ring.desc[slot] = more ? make_int4(it.bh, it.q0, it.n, it.tok0) : make_int4(-1, 0, 0, 0);
-                    mbar_arrive(smem_u32(&ring.full[slot]));
+                    ring->desc[slot] = more ? make_int4(it.bh, it.q0, it.n, it.tok0) : make_int4(-1, 0, 0, 0);
+                    mbar_arrive(smem_u32(&ring->full[slot]));
                 }
                 __syncwarp();
             }
@@ -361,137 +374,180 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_inc<192>();
         // -------------------------------------------------------------- softmax + epilogue
-        const int t = warp >> 2;
+        constexpr int HK = kBK128 / 2;  // keys per half
+        constexpr int HD = D / 2;       // O columns per half
+        const int h = warp >> 2;        // key half of this warpgroup
+        const int qd = warp & 3;        // TMEM lane quadrant (warps qd and qd + 4 share it)
         const int r = threadIdx.x & 127;
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + 128 * t;
-        const uint32_t p_addr = tmem + lane_base + C::TM_P + C::TM_P_STRIDE * t;
-        const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const float scale_log2 = p.scale_log2;
         // raw scores scaled inside the exponent when the scale is positive (the maximum
         // commutes with it); otherwise pre-scaled scores (a -inf raw score times a
         // non-positive scale is not -inf)
         const bool fast = scale_log2 > 0.0f;
         const float sl2 = fast ? scale_log2 : 1.0f;
-        uint32_t scount = 0;  // S blocks consumed (all items)
-        uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
+        uint32_t xcount = 0;  // exchanges with the partner thread (phase of the pair's barrier)
+        // The partner (same row, other key half) receives v; returns the partner's value. The
+        // pair meets at an mbarrier with the same bounded wait as every pipeline wait (a warp
+        // that gives up does not leave its partner waiting forever). Buffers alternate by
+        // phase: a value is overwritten two exchanges later, after the partner has read it.
+        const uint32_t pair_bar = smem_u32(xbar + qd);
+        auto exchange = [&](float v, bool &okx) -> float {
+            float *buf = xch + (xcount & 1u) * 256;
+            buf[h * 128 + r] = v;
+            tc_fence_before();  // this thread's tensor-memory reads come before the partner's writes
+            mbar_arrive(pair_bar);
+            okx = wait_warp(pair_bar, xcount & 1u, abort_flag, p);
+            ++xcount;
+            tc_fence_after();
+            return buf[(h ^ 1) * 128 + r];
+        };
+        uint32_t scount[2] = {0, 0};  // S blocks consumed per tile (all items)
+        uint32_t g[2] = {0, 0};       // P blocks produced per tile = its P V products
         bool ok = true;
-        ItemIter<VARLEN> iter(p, abort_flag);
+        ItemIter<VARLEN> iter(p, abort_flag, ring);
         for (Item itm; ok && iter.next(p, itm, ok);) {
             const int bh = itm.bh, q0 = itm.q0, n = itm.n;
-            const int nt = tile_nkv<CAUSAL, kBK128>(itm, t);
-            if (nt == 0) continue;
-            const int row = q0 + t * kBQ + r;  // query row within the sequence (may be >= n in a ragged tail)
-            const int tile_row0 = q0 + t * kBQ;
-            float m_ref = -INFINITY, l = 0.0f;
-            for (int j = 0; j < nt; ++j, ++g) {
-                ok = wait_warp(sy.s_full(t), scount & 1u, abort_flag, p);
-                ++scount;
-                if (!ok) break;
-                tc_fence_after();
-                float x[128];
-                {
-                    uint32_t sr[128];
-                    tmem_ld128_wait(s_addr, sr);
+            const int nt[2] = {tile_nkv<CAUSAL, kBK128>(itm, 0), tile_nkv<CAUSAL, kBK128>(itm, 1)};
+            const int nmax = max(nt[0], nt[1]);
+            float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+            for (int j = 0; ok && j < nmax; ++j) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) x[c] = fast ? __uint_as_float(sr[c]) : __uint_as_float(sr[c]) * scale_log2;
-                }
-                if constexpr (!C::ALIAS) {
-                    tc_fence_before();
-                    mbar_arrive(sy.s_free(t));  // S_t may now be overwritten by the next block
-                }
-                // keys past the end of the sequence, and (causal) keys after the query
-                const int kbase = j * kBK128;
-                const bool ragged = kbase + kBK128 > n;
-                const bool diag = CAUSAL && (kbase + kBK128 - 1 > tile_row0);
-                if (ragged || diag) {
-                    int lim = n - 1 - kbase;
-                    if (CAUSAL) lim = min(lim, row - kbase);
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || j >= nt[t]) continue;
+                    const uint32_t s_addr = tmem + lane_base + 128 * t + HK * h;  // fp32 S columns of this half
+                    const uint32_t p_addr = tmem + lane_base + C::TM_P + C::TM_P_STRIDE * t + HK / 2 * h;
+                    const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t + HD * h;
+                    ok = wait_warp(sy.s_full(t), scount[t] & 1u, abort_flag, p);
+                    ++scount[t];
+                    if (!ok) break;
+                    tc_fence_after();
+                    float x[HK];
+                    {
+                        uint32_t sr[HK];
+                        tmem_ld64_nowait(s_addr, sr);
+                        tmem_wait_ld_dep64(sr);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
-                }
-                const float mb = row_max128(x) * sl2;  // sl2 > 0
-                const float m_new = fmaxf(m_ref, mb);
-                // lazy rescale: move the reference only when the maximum grew by more than TAU
-                const bool need = (m_new > m_ref + kTau) || (m_ref == -INFINITY && m_new != -INFINITY);
-                const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;  // 2^-inf = 0
-                const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
-                if (need) {
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-                const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-                const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
-                float2 ls[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                                make_float2(0.0f, 0.0f)};
-                // P in two halves of 64 keys (32 packed columns each), each stored as soon as it is ready
+                        for (int c = 0; c < HK; ++c)
+                            x[c] = fast ? __uint_as_float(sr[c]) : __uint_as_float(sr[c]) * scale_log2;
+                    }
+                    if constexpr (!C::ALIAS) {
+                        tc_fence_before();
+                        mbar_arrive(sy.s_free(t));  // S_t may now be overwritten by the next block
+                    }
+                    // keys past the end of the sequence, and (causal) keys after the query
+                    const int row = q0 + t * kBQ + r;  // query row within the sequence (may be >= n)
+                    const int kbase = j * kBK128 + HK * h;
+                    const bool ragged = kbase + HK > n;
+                    const bool diag = CAUSAL && (kbase + HK - 1 > q0 + t * kBQ);
+                    if (ragged || diag) {
+                        int lim = n - 1 - kbase;
+                        if (CAUSAL) lim = min(lim, row - kbase);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pv[32];
+                        for (int c = 0; c < HK; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
+                    }
+                    float m8[8];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int i = 64 * h + 2 * c;
-                        const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
+                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[24 + i], x[32 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[40 + i], x[48 + i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[56 + i]);
+                    const float mhalf =
+                        fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                    const float mother = exchange(mhalf, ok);
+                    if (!ok) break;
+                    const float mb = fmaxf(mhalf, mother) * sl2;  // sl2 > 0
+                    const float m_new = fmaxf(m_ref[t], mb);
+                    // lazy rescale: move the reference only when the maximum grew by more than TAU
+                    const bool need = (m_new > m_ref[t] + kTau) || (m_ref[t] == -INFINITY && m_new != -INFINITY);
+                    const float alpha = need ? ex2_approx(m_ref[t] - m_new) : 1.0f;  // 2^-inf = 0
+                    const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
+                    if (need) {
+                        l[t] *= alpha;
+                        m_ref[t] = m_new;
+                    }
+                    const float neg = (m_ref[t] == -INFINITY) ? 0.0f : -m_ref[t];
+                    const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
+                    float2 ls[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                    make_float2(0.0f, 0.0f)};
+                    uint32_t pv[HK / 2];
+#pragma unroll
+                    for (int c = 0; c < HK / 2; ++c) {
+                        const float2 a = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sl2v, negv);
                         const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                         ls[c & 3] = fadd2(ls[c & 3], e);
                         pv[c] = pack2<T>(e.x, e.y);
                     }
-                    // Before the first store, the previous block's P V product must be complete:
-                    // it read P_t (D = 64: P_t's own buffer) and it is the last product in O_t
-                    // before a rescale. D = 128: it was issued before S(j) by the same thread, so
-                    // it is complete already and the wait only keeps the phases in step.
-                    if (h == 0 && j > 0) {
-                        ok = wait_warp(sy.pv_done(t), (g - 1) & 1u, abort_flag, p);
+                    l[t] += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+                    // Before the store, the previous block's P V product must be complete: it read
+                    // P_t (D = 64: P_t's own buffer) and it is the last product in O_t before a
+                    // rescale. D = 128: it was issued before S(j) by the same thread, so it is
+                    // complete already and the wait only keeps the phases in step. (The P of the
+                    // second half lands on S columns of the first half, which the partner copied
+                    // out before it reached the exchange.)
+                    if (j > 0) {
+                        ok = wait_warp(sy.pv_done(t), (g[t] - 1) & 1u, abort_flag, p);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    tmem_st32(p_addr + 32 * h, pv);
+                    tmem_st32(p_addr, pv);
+                    if (rescale) {
+                        // O holds P V for blocks < j relative to the old reference: scale this half's
+                        // columns of the row (alpha = 1 where the reference did not move)
+#pragma unroll
+                        for (int c0 = 0; c0 < HD; c0 += 32) {
+                            uint32_t ov[32];
+                            tmem_ld32_wait(o_addr + c0, ov);
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                            tmem_st32(o_addr + c0, ov);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(sy.p_full(t));
+                    ++g[t];
                 }
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue, tile by tile
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!ok || nt[t] == 0) continue;
+                const float l_other = exchange(l[t], ok);  // the other half's partial denominator
                 if (!ok) break;
-                l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-                if (rescale) {
-                    // O holds P V for blocks < j relative to the old reference: scale its rows
-                    // (alpha = 1 for rows whose reference did not move) before P V(j) adds to it
+                const float l_row = l[t] + l_other;
+                ok = wait_warp(sy.pv_done(t), (g[t] - 1) & 1u, abort_flag, p);
+                if (!ok) break;
+                tc_fence_after();
+                const int row = q0 + t * kBQ + r;
+                const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t + HD * h;
+                const float inv = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
+                const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
+                                               : ((size_t)bh * p.N + (size_t)row);
+                T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D + HD * h;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t ov[32];
-                        tmem_ld32_wait(o_addr + c0, ov);
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32_wait(o_addr + c0, ov);
+                    if (row < n) {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                        tmem_st32(o_addr + c0, ov);
+                        for (int c = 0; c < 32; c += 8)
+                            st_global_v4(orow + c0 + c,
+                                         pack2<T>(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv),
+                                         pack2<T>(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv),
+                                         pack2<T>(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv),
+                                         pack2<T>(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv));
                     }
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(sy.p_full(t));
+                tc_fence_before();  // the O reads come before the next item's first P V (after p_full)
+                if (h == 0 && row < n)
+                    p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
+                        (l_row > 0.0f) ? (m_ref[t] + lg2_approx(l_row)) * 0.6931471805599453f : -INFINITY;
             }
-            if (!ok) break;
-            // ---------------------------------------------------------- epilogue
-            ok = wait_warp(sy.pv_done(t), (g - 1) & 1u, abort_flag, p);
-            if (!ok) break;
-            tc_fence_after();
-            const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
-            const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
-                                           : ((size_t)bh * p.N + (size_t)row);
-            T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32_wait(o_addr + c0, ov);
-                if (row < n) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 8)
-                        st_global_v4(orow + c0 + c,
-                                     pack2<T>(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv),
-                                     pack2<T>(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv),
-                                     pack2<T>(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv),
-                                     pack2<T>(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv));
-                }
-            }
-            tc_fence_before();  // the O reads above come before the next item's first P V (after p_full)
-            if (row < n)
-                p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
-                    (l > 0.0f) ? (m_ref + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
         }
     }
 

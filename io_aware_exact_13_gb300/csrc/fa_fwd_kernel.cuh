@@ -330,10 +330,12 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 template <bool VARLEN>
 struct ItemIter;
 
+struct ItemRing;
+
 template <>
 struct ItemIter<false> {
     int w = 0;
-    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *) {}
+    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *, ItemRing * = nullptr) {}
     __device__ __forceinline__ bool next(const FwdParams &p, Item &it, bool &) {
         const int item = item_at(p, w++);
         if (item < 0) return false;
@@ -372,10 +374,12 @@ template <>
 struct ItemIter<true> {
     uint32_t i = 0;
     volatile int *abort_flag;
-    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *abort) : abort_flag(abort) {}
+    ItemRing *ring_ptr;  // the CTA's ring (static shared memory, or a slot of the dynamic region)
+    __device__ __forceinline__ ItemIter(const FwdParams &, volatile int *abort, ItemRing *ring)
+        : abort_flag(abort), ring_ptr(ring) {}
     // false at the end of the list; a wait that gives up also clears ok
     __device__ __forceinline__ bool next(const FwdParams &p, Item &it, bool &ok) {
-        ItemRing &ring = item_ring();
+        ItemRing &ring = *ring_ptr;
         const uint32_t slot = i % kItemRing;
         if (!wait_warp(smem_u32(&ring.full[slot]), (i / kItemRing) & 1u, abort_flag, p)) {
             ok = false;
@@ -394,6 +398,13 @@ struct ItemIter<true> {
         return true;
     }
 };
+
+// The item ring of the 64-key kernel (static shared memory; packed batches only).
+template <bool VARLEN>
+__device__ __forceinline__ ItemRing *static_item_ring() {
+    if constexpr (VARLEN) return &item_ring();
+    else return nullptr;
+}
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);
@@ -507,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pos;
                 return true;
             };
-            ItemIter<VARLEN> iter(p, abort_flag);
+            ItemIter<VARLEN> iter(p, abort_flag, static_item_ring<VARLEN>());
             for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int q0 = itm.q0, cur_bh = itm.bh;
                 // grouped-query attention: kv_group consecutive query heads share one K/V head
@@ -571,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t KVT16 = C::KV_TILE >> 4;
             uint32_t qcount = 0, s_issued = 0, kpos = 0;
             bool ok = true;
-            ItemIter<VARLEN> iter(p, abort_flag);
+            ItemIter<VARLEN> iter(p, abort_flag, static_item_ring<VARLEN>());
             for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int nt = tile_nkv<CAUSAL>(itm, t);
                 const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
@@ -616,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t KVT16 = C::KV_TILE >> 4;
             uint32_t g = 0, vpos = 0;
             bool ok = true;
-            ItemIter<VARLEN> iter(p, abort_flag);
+            ItemIter<VARLEN> iter(p, abort_flag, static_item_ring<VARLEN>());
             for (Item itm; ok && iter.next(p, itm, ok);) {
                 const int nt = tile_nkv<CAUSAL>(itm, t);
                 const int nmax = max(tile_nkv<CAUSAL>(itm, 0), tile_nkv<CAUSAL>(itm, 1));
@@ -687,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t scount = 0;  // S blocks consumed (all items)
         uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
         bool ok = true;
-        ItemIter<VARLEN> iter(p, abort_flag);
+        ItemIter<VARLEN> iter(p, abort_flag, static_item_ring<VARLEN>());
         for (Item itm; ok && iter.next(p, itm, ok);) {
             const int bh = itm.bh, q0 = itm.q0, n = itm.n;
             const int nt = tile_nkv<CAUSAL>(itm, t);

@@ -409,51 +409,60 @@ def simulate_bwd_halves(n_it, stages, seed):
     return True
 
 
-def simulate_bk128(N, causal, items, rk, rv, seed, alias, softmax_warps=4, rescale_prob=0.1, item_ring=0,
-                   in_order_pv_then_s=True, pv_wait_every_block=True):
+def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item_ring=0,
+                   in_order_pv_then_s=True, pv_wait_every_block=True, exchange_before_p=True):
     """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
-    one issuing warp per query tile (S_t and P_t V products), the softmax warps of
-    both tiles, and (``item_ring`` > 0) the packed-batch item list.
+    one issuing warp per query tile (S_t and P_t V products), the eight softmax
+    warps and (``item_ring`` > 0) the packed-batch item list.
+
+    The softmax warps work on one tile at a time: warp w = 4 h + q takes key half h
+    of TMEM lane quadrant q, for tile 0 then tile 1 of each block; warps q and
+    q + 4 (the same rows) exchange their row maxima at a pair barrier before
+    computing P, and their partial denominators at the epilogue.
 
     ``alias`` is the d = 128 layout, where P_t is written over S_t's tensor-memory
-    columns: the issuer orders O += P V(j) before S(j+1). Besides the barrier
-    checks of ``simulate`` this model tracks what each tile's S/P columns and P
-    buffer hold, so that a product that overwrites P before the P V product has
-    read it, or a softmax that reads S before it is complete, fails here.
-    ``in_order_pv_then_s=False`` is an aliasing issuer that issues S(j+1) before
-    P V(j) (it must be caught); ``pv_wait_every_block=False`` is a softmax that
-    skips its per-block wait for the previous P V commit (the epilogue's parity
-    wait then can alias, which must be caught too)."""
+    columns (key half h of P over S columns [32 h, 32 h + 32), which belong to
+    half 0): the issuer orders O += P V(j) before S(j+1). Besides the barrier
+    checks of ``simulate`` this model tracks what each 32-column quarter of each
+    lane quadrant holds, so that a product that overwrites P before the P V
+    product has read it, a P written over S columns that their owner has not
+    copied out, or a softmax that reads S before it is complete, fails here.
+    Mutations that must be caught: ``in_order_pv_then_s=False`` (an aliasing
+    issuer that issues S(j+1) before P V(j)), ``pv_wait_every_block=False`` (at
+    d = 64, a softmax that stores P(j) before P V(j-1) has read its buffer),
+    ``exchange_before_p=False`` (half 1 writes its P before the pair exchange,
+    over S columns half 0 may not have copied out)."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
+    NW = 8
 
     def bar(name, count):
         B[name] = Bar(name, count)
 
     for t in range(2):
-        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", BQ), ("p_full", BQ),
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", 2 * BQ), ("p_full", 2 * BQ),
                         ("pv_done", 1)):
             bar(f"{name}{t}", c)
-    for s in range(rk):
-        bar(f"k_full{s}", 1)
-        bar(f"k_empty{s}", 2)
-    for s in range(rv):
-        bar(f"v_full{s}", 1)
-        bar(f"v_empty{s}", 2)
-    consumers = 3 + 2 * softmax_warps
-    for s in range(item_ring):
-        bar(f"item_full{s}", 1)
-        bar(f"item_empty{s}", consumers)
+    for s_ in range(rk):
+        bar(f"k_full{s_}", 1)
+        bar(f"k_empty{s_}", 2)
+    for s_ in range(rv):
+        bar(f"v_full{s_}", 1)
+        bar(f"v_empty{s_}", 2)
+    for q in range(4):
+        bar(f"x{q}", 64)
+    consumers = 3 + NW
+    for s_ in range(item_ring):
+        bar(f"item_full{s_}", 1)
+        bar(f"item_empty{s_}", consumers)
     tensor_pipe, tma = [], []
-    # tensor-memory contents per tile: the S columns ("S", j) / ("P", j) and, without aliasing, the P buffer
-    # (per softmax warp: each warp owns 32 of the 128 lanes; a product writes or reads all of them)
-    scols = [[None] * softmax_warps for _ in range(2)]
-    pbuf = [[None] * softmax_warps for _ in range(2)]
-    sread = [set(), set()]      # S blocks the softmax has finished copying out (all its warps)
-    sreaders = [{}, {}]
-    pv_read = [set(), set()]    # P blocks whose P V product has executed
-    o_last = [None, None]       # the last P V product that wrote O_t
+    # per tile, lane quadrant and 32-column quarter of S_t: ("S", g, owner_has_read) or ("P", g)
+    scols = [[[None] * 4 for _ in range(4)] for _ in range(2)]
+    pbuf = [[[None] * 2 for _ in range(4)] for _ in range(2)]  # d = 64: P_t's own buffer, per half
+    sread_count = [{}, {}]   # S block -> quarters copied out
+    pv_read = [set(), set()]
+    o_last = [None, None]
 
     def nkv(n_seq, q0, t):
         r0 = q0 + t * BQ
@@ -510,30 +519,30 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, softmax_warps=4, resca
         st = {"q": 0, "k": 0, "v": 0, "p": 0, "s": 0}
 
         def issue_s(j, nt, gidx):
-            s = st["k"] % rk
-            yield ("wait", f"k_full{s}", st["k"] // rk)
+            s_ = st["k"] % rk
+            yield ("wait", f"k_full{s_}", st["k"] // rk)
             st["k"] += 1
             if j >= nt:
-                yield ("arrive", f"k_empty{s}", 1)
+                yield ("arrive", f"k_empty{s_}", 1)
                 return
             if not alias and st["s"] > 0:
                 yield ("wait", f"s_free{t}", st["s"] - 1)
             st["s"] += 1
             tensor_pipe.extend([("mma", "S", t, gidx), ("commit", f"s_full{t}")]
-                               + ([("commit", f"q_empty{t}")] if j == nt - 1 else []) + [("commit", f"k_empty{s}")])
+                               + ([("commit", f"q_empty{t}")] if j == nt - 1 else []) + [("commit", f"k_empty{s_}")])
 
         def issue_pv(j, nt, gidx):
-            s = st["v"] % rv
-            yield ("wait", f"v_full{s}", st["v"] // rv)
+            s_ = st["v"] % rv
+            yield ("wait", f"v_full{s_}", st["v"] // rv)
             st["v"] += 1
             if j >= nt:
-                yield ("arrive", f"v_empty{s}", 1)
+                yield ("arrive", f"v_empty{s_}", 1)
                 return
             yield ("wait", f"p_full{t}", st["p"])
             st["p"] += 1
-            tensor_pipe.extend([("mma", "PV", t, gidx), ("commit", f"pv_done{t}"), ("commit", f"v_empty{s}")])
+            tensor_pipe.extend([("mma", "PV", t, gidx), ("commit", f"pv_done{t}"), ("commit", f"v_empty{s_}")])
 
-        g0 = 0  # index of the tile's first block of the item among all its blocks
+        g0 = 0
         for i, q0 in enumerate(items):
             yield from take(i)
             n, nmax = counts(q0)
@@ -556,60 +565,84 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, softmax_warps=4, resca
             g0 += nt
         yield from take(len(items))
 
-    def softmax(t, w):
-        scount = g = 0
+    def softmax(w):
+        h, q = w // 4, w % 4
+        scount, g, xcount = [0, 0], [0, 0], 0
+
+        def store_p(t):
+            if alias:  # half h of P over quarter h, owned by half 0
+                cell = scols[t][q][h]
+                assert cell is not None and cell[0] == "S" and cell[1] == g[t] and cell[2], (
+                    f"tile {t}: P({g[t]}) half {h} written over {cell} (not yet copied out)")
+                scols[t][q][h] = ("P", g[t])
+            else:
+                cell = pbuf[t][q][h]
+                assert cell is None or cell[1] in pv_read[t], (
+                    f"tile {t}: P({g[t]}) overwrites P{cell} before its P V product read it")
+                pbuf[t][q][h] = ("P", g[t])
+
         for i, q0 in enumerate(items):
             yield from take(i)
-            n, _ = counts(q0)
-            nt = n[t]
-            if not nt:
-                continue
-            for j in range(nt):
-                yield ("wait", f"s_full{t}", scount)
-                scount += 1
-                assert scols[t][w] == ("S", g), f"tile {t}: softmax reads S({g}) but the columns hold {scols[t][w]}"
-                sreaders[t][g] = sreaders[t].get(g, 0) + 1
-                if sreaders[t][g] == softmax_warps:
-                    sread[t].add(g)
-                if not alias:
-                    yield ("arrive", f"s_free{t}", BQ // softmax_warps)
-                if j > 0 and (pv_wait_every_block or rnd.random() < rescale_prob):
-                    yield ("wait", f"pv_done{t}", g - 1)
-                # store P(g)
-                if alias:
-                    assert scols[t][w] == ("S", g), f"tile {t}: P({g}) written over {scols[t][w]}"
-                    scols[t][w] = ("P", g)
-                else:
-                    assert pbuf[t][w] is None or pbuf[t][w][1] in pv_read[t], (
-                        f"tile {t}: P({g}) overwrites P{pbuf[t][w]} before its P V product read it")
-                    pbuf[t][w] = ("P", g)
-                yield ("arrive", f"p_full{t}", BQ // softmax_warps)
-                g += 1
-            yield ("wait", f"pv_done{t}", g - 1)  # epilogue
-            assert o_last[t] == g - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]}) of the next item"
+            n, nmax = counts(q0)
+            for j in range(nmax):
+                for t in range(2):
+                    if j >= n[t]:
+                        continue
+                    yield ("wait", f"s_full{t}", scount[t])
+                    scount[t] += 1
+                    for c in (2 * h, 2 * h + 1):
+                        cell = scols[t][q][c]
+                        assert cell is not None and cell[:2] == ("S", g[t]), (
+                            f"tile {t}: softmax reads S({g[t]}) but quarter {c} holds {cell}")
+                        scols[t][q][c] = ("S", g[t], True)
+                    if not alias:
+                        yield ("arrive", f"s_free{t}", 32)
+                    if not exchange_before_p:
+                        store_p(t)
+                    yield ("arrive", f"x{q}", 32)
+                    yield ("wait", f"x{q}", xcount)
+                    xcount += 1
+                    if j > 0 and (pv_wait_every_block or rnd.random() < rescale_prob):
+                        yield ("wait", f"pv_done{t}", g[t] - 1)
+                    if exchange_before_p:
+                        store_p(t)
+                    yield ("arrive", f"p_full{t}", 32)
+                    g[t] += 1
+            for t in range(2):
+                if not n[t]:
+                    continue
+                yield ("arrive", f"x{q}", 32)
+                yield ("wait", f"x{q}", xcount)
+                xcount += 1
+                yield ("wait", f"pv_done{t}", g[t] - 1)  # epilogue
+                assert o_last[t] == g[t] - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]})"
         yield from take(len(items))
 
     def execute(kind, t, g):
         if kind == "S":
-            for prev in scols[t]:
-                if alias:  # the columns must hold a P whose P V product has read it
-                    assert prev is None or (prev[0] == "P" and prev[1] in pv_read[t]), (
-                        f"tile {t}: S({g}) overwrites {prev} before it was consumed")
-                else:
-                    assert prev is None or prev[1] in sread[t], f"tile {t}: S({g}) overwrites S{prev} before it was read"
-            scols[t] = [("S", g)] * softmax_warps
+            for q in range(4):
+                for c in range(4):
+                    prev = scols[t][q][c]
+                    if prev is None:
+                        continue
+                    if prev[0] == "P":
+                        assert prev[1] in pv_read[t], f"tile {t}: S({g}) overwrites {prev} before its P V read it"
+                    else:
+                        assert len(prev) == 3 and prev[2], f"tile {t}: S({g}) overwrites S{prev} before it was read"
+            scols[t] = [[("S", g, False)] * 4 for _ in range(4)]
         else:
-            for held in (scols[t] if alias else pbuf[t]):
-                assert held == ("P", g), f"tile {t}: P V({g}) reads {held}"
+            for q in range(4):
+                held = scols[t][q][:2] if alias else pbuf[t][q]
+                for cell in held:
+                    assert cell == ("P", g), f"tile {t}: P V({g}) reads {cell}"
             pv_read[t].add(g)
             o_last[t] = g
 
     agents = {"producer": producer(), "I0": issuer(0), "I1": issuer(1)}
     if item_ring:
         agents["scheduler"] = scheduler()
-    for t in range(2):
-        for w in range(softmax_warps):
-            agents[f"softmax{t}.{w}"] = softmax(t, w)
+    for w in range(NW):
+        agents[f"softmax{w}"] = softmax(w)
     waiting = {k: None for k in agents}
     while agents or tensor_pipe or tma:
         ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]

@@ -177,3 +177,17 @@ def test_bk128_skipping_the_per_block_commit_wait_is_caught():
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+def test_bk128_p_before_the_exchange_is_caught():
+    """d = 128: the second key half's P lands on S columns of the first half; writing
+    it before the pair exchange (before the first half has copied them out): caught."""
+    from pipeline_model import simulate_bk128
+
+    caught = 0
+    for seed in range(20):
+        try:
+            simulate_bk128(1000, True, _items128(1000, True), 3, 2, seed, True, exchange_before_p=False)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
