@@ -85,8 +85,8 @@ struct Cfg128 {
     static constexpr int SMEM_V = SMEM_K + RK * KV_TILE;
     static constexpr int SMEM_BAR = SMEM_V + RV * KV_TILE;
     // q_full[2] q_empty[2] k_full[RK] k_empty[RK] v_full[RV] v_empty[RV] s_full[2] s_free[2] p_full[2]
-    // pv_done[2] drain
-    static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 8 + 1;
+    // pv_done[2][2] drain
+    static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 10 + 1;
     static constexpr int SMEM_TMEM_SLOT = SMEM_BAR + ((NUM_BARS * 8 + 15) / 16) * 16;
     static constexpr int SMEM_XBAR = SMEM_TMEM_SLOT + 16;         // 4 exchange barriers (one per lane quadrant)
     static constexpr int SMEM_XCH = SMEM_XBAR + 32;               // float [2 parity][2 halves][128 rows]
@@ -113,14 +113,14 @@ struct Sync128 {
     __device__ __forceinline__ uint32_t k_empty(int s) const { return at(4 + RK + s); }
     __device__ __forceinline__ uint32_t v_full(int s) const { return at(4 + 2 * RK + s); }
     __device__ __forceinline__ uint32_t v_empty(int s) const { return at(4 + 2 * RK + RV + s); }
-    // Per tile: S ready (MMA commit), S copied out (D = 64 only), P ready (128 softmax
-    // threads), P V done (MMA commit). Every waiter waits on every phase in turn, and
-    // no signaller can get two phases ahead of its waiter (see the roles below).
+    // Per tile: S ready (MMA commit), S copied out (D = 64 only), P ready (256 softmax
+    // threads), P V(g) done (MMA commit to pv_done(t, g & 1)). No barrier can get two
+    // phases ahead of a waiter (see the roles below), so parity waits are exact.
     __device__ __forceinline__ uint32_t s_full(int t) const { return at(B0 + t); }
     __device__ __forceinline__ uint32_t s_free(int t) const { return at(B0 + 2 + t); }
     __device__ __forceinline__ uint32_t p_full(int t) const { return at(B0 + 4 + t); }
-    __device__ __forceinline__ uint32_t pv_done(int t) const { return at(B0 + 6 + t); }
-    __device__ __forceinline__ uint32_t drain() const { return at(B0 + 8); }
+    __device__ __forceinline__ uint32_t pv_done(int t, int b) const { return at(B0 + 6 + 2 * t + b); }
+    __device__ __forceinline__ uint32_t drain() const { return at(B0 + 10); }
 };
 
 template <typename T, int D, bool CAUSAL, bool VARLEN>
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.s_full(t), 1);
             mbar_init(sy.s_free(t), 2 * kBQ);  // both softmax warpgroups
             mbar_init(sy.p_full(t), 2 * kBQ);
-            mbar_init(sy.pv_done(t), 1);
+            mbar_init(sy.pv_done(t, 0), 1);
+            mbar_init(sy.pv_done(t, 1), 1);
         }
         for (int s = 0; s < RK; ++s) {  // a slot is released by both tiles' issuers
             mbar_init(sy.k_full(s), 1);
@@ -274,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------------------------------------------------- issuer of tile t
             // The whole warp runs the loop (warp-uniform), lane 0 issues.
             //   S_t(j)  = Q_t K_j^T     into S_t's columns, committed to s_full(t)
-            //   O_t    (+)= P_t(j) V_j  once the softmax has written P_t(j), committed to pv_done(t)
+            //   O_t    (+)= P_t(j) V_j  once the softmax has written P_t(j); the g-th product of the
+            //                            tile is committed to pv_done(t, g & 1)
             // D = 128: P V(j) then S(j+1) (P_t lives in S_t's columns, in-order products).
             // D = 64:  S(j+1) as soon as the softmax has copied S(j) out, then P V(j).
             // K and V slots of blocks this tile does not need are released at once.
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < C::KSTEPS_PV; ++k)
                     mma_ts(d_o, a_p + k * 8, b0 + (uint64_t)((k * C::V_KSTEP_BYTES) >> 4), C::IDESC_PV,
                            (k > 0 || j > 0) ? 1u : 0u, issue);
-                tc_commit(sy.pv_done(t), issue);
+                tc_commit(sy.pv_done(t, (pcount - 1) & 1u), issue);
                 tc_commit(sy.v_empty(slot), issue);
                 return true;
             };
@@ -482,19 +484,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pv[c] = pack2<T>(e.x, e.y);
                     }
                     l[t] += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-                    // Before the store, the previous block's P V product must be complete: it read
-                    // P_t (D = 64: P_t's own buffer) and it is the last product in O_t before a
-                    // rescale. D = 128: it was issued before S(j) by the same thread, so it is
-                    // complete already and the wait only keeps the phases in step. (The P of the
-                    // second half lands on S columns of the first half, which the partner copied
-                    // out before it reached the exchange.)
-                    if (j > 0) {
-                        ok = wait_warp(sy.pv_done(t), (g[t] - 1) & 1u, abort_flag, p);
+                    // P V(g-1), the tile's previous product, read P_t and accumulated into O_t. Its
+                    // commit can reach pv_done several hundred cycles after the commit of S(g), which
+                    // was issued after it, so the softmax waits for it only where it must:
+                    //  D = 64:  before storing P, which reuses P_t's buffer;
+                    //  D = 128: before rescaling O. P(g) goes over S(g)'s columns, which the tensor
+                    //           core wrote after P V(g-1) had read P(g-1) there (it runs one issuing
+                    //           thread's products in order), and the softmax stores only after it
+                    //           has seen S(g) complete. (The P of the second key half lands on S
+                    //           columns of the first half, which the partner copied out before the
+                    //           exchange.)
+                    // Besides, P V(g-2) (long complete) is waited for before P(g) is released, so
+                    // that neither pv_done barrier can get two phases ahead of these waits.
+                    auto wait_pv = [&](uint32_t gg) -> bool {
+                        return wait_warp(sy.pv_done(t, gg & 1u), (gg >> 1) & 1u, abort_flag, p);
+                    };
+                    if (!C::ALIAS && g[t] > 0) {
+                        ok = wait_pv(g[t] - 1);
                         if (!ok) break;
                         tc_fence_after();
                     }
                     tmem_st32(p_addr, pv);
                     if (rescale) {
+                        if (C::ALIAS) {
+                            ok = wait_pv(g[t] - 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
                         // O holds P V for blocks < j relative to the old reference: scale this half's
                         // columns of the row (alpha = 1 where the reference did not move)
 #pragma unroll
@@ -505,6 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
                             tmem_st32(o_addr + c0, ov);
                         }
+                    }
+                    if (C::ALIAS && g[t] >= 2) {
+                        ok = wait_pv(g[t] - 2);
+                        if (!ok) break;
                     }
                     tmem_wait_st();
                     tc_fence_before();
@@ -520,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float l_other = exchange(l[t], ok);  // the other half's partial denominator
                 if (!ok) break;
                 const float l_row = l[t] + l_other;
-                ok = wait_warp(sy.pv_done(t), (g[t] - 1) & 1u, abort_flag, p);
+                ok = wait_warp(sy.pv_done(t, (g[t] - 1) & 1u), ((g[t] - 1) >> 1) & 1u, abort_flag, p);
                 if (!ok) break;
                 tc_fence_after();
                 const int row = q0 + t * kBQ + r;

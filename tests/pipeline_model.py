@@ -35,6 +35,11 @@ class Bar:
         assert index < 0 or self.phase <= index + 1, (
             f"{self.name}: waiting for completion {index} while the barrier is at phase {self.phase} "
             "(the parity wait would alias)")
+        # a parity wait succeeds when the phase count's parity differs from the awaited one's: too
+        # early if the barrier is an odd number of completions short of the awaited one
+        assert index < 0 or self.phase >= index or not ((self.phase ^ index) & 1), (
+            f"{self.name}: waiting for completion {index} while only {self.phase} completed "
+            "(the parity wait would succeed early)")
         return self.phase > index
 
 
@@ -410,7 +415,8 @@ def simulate_bwd_halves(n_it, stages, seed):
 
 
 def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item_ring=0,
-                   in_order_pv_then_s=True, pv_wait_every_block=True, exchange_before_p=True):
+                   in_order_pv_then_s=True, pv_wait_every_block=True, exchange_before_p=True,
+                   lag2_wait=True, rescale_wait=True, late_weight=1.0):
     """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
     one issuing warp per query tile (S_t and P_t V products), the eight softmax
     warps and (``item_ring`` > 0) the packed-batch item list.
@@ -427,11 +433,22 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     lane quadrant holds, so that a product that overwrites P before the P V
     product has read it, a P written over S columns that their owner has not
     copied out, or a softmax that reads S before it is complete, fails here.
+    The commits of P V products (to pv_done(t, g & 1)) may reach their barriers
+    late, after the commits of products issued after them (measured on the GPU:
+    several hundred cycles after the next S), but in order among themselves
+    (``late_weight`` < 1 makes the scheduler deliver them rarely, so that they lag
+    by several products); a P V
+    product's accumulation into O counts as done only when its commit arrives, and
+    the softmax may rescale or read O only after every earlier product is done.
+
     Mutations that must be caught: ``in_order_pv_then_s=False`` (an aliasing
     issuer that issues S(j+1) before P V(j)), ``pv_wait_every_block=False`` (at
     d = 64, a softmax that stores P(j) before P V(j-1) has read its buffer),
     ``exchange_before_p=False`` (half 1 writes its P before the pair exchange,
-    over S columns half 0 may not have copied out)."""
+    over S columns half 0 may not have copied out), ``lag2_wait=False`` (d = 128
+    without the wait for P V(g-2): a barrier runs two phases ahead of a later
+    wait), ``rescale_wait=False`` (d = 128, O rescaled without waiting for
+    P V(g-1))."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
@@ -442,7 +459,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
 
     for t in range(2):
         for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", 2 * BQ), ("p_full", 2 * BQ),
-                        ("pv_done", 1)):
+                        ("pv_done0", 1), ("pv_done1", 1)):
             bar(f"{name}{t}", c)
     for s_ in range(rk):
         bar(f"k_full{s_}", 1)
@@ -457,6 +474,8 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
         bar(f"item_full{s_}", 1)
         bar(f"item_empty{s_}", consumers)
     tensor_pipe, tma = [], []
+    late = [[], []]          # per tile: P V commits executed but not yet arrived (in order)
+    o_done = [-1, -1]        # per tile: the last P V product whose commit has arrived
     # per tile, lane quadrant and 32-column quarter of S_t: ("S", g, owner_has_read) or ("P", g)
     scols = [[[None] * 4 for _ in range(4)] for _ in range(2)]
     pbuf = [[[None] * 2 for _ in range(4)] for _ in range(2)]  # d = 64: P_t's own buffer, per half
@@ -540,7 +559,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                 return
             yield ("wait", f"p_full{t}", st["p"])
             st["p"] += 1
-            tensor_pipe.extend([("mma", "PV", t, gidx), ("commit", f"pv_done{t}"), ("commit", f"v_empty{s_}")])
+            tensor_pipe.extend([("mma", "PV", t, gidx), ("late", t, gidx), ("commit", f"v_empty{s_}")])
 
         g0 = 0
         for i, q0 in enumerate(items):
@@ -602,10 +621,20 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                     yield ("arrive", f"x{q}", 32)
                     yield ("wait", f"x{q}", xcount)
                     xcount += 1
-                    if j > 0 and (pv_wait_every_block or rnd.random() < rescale_prob):
-                        yield ("wait", f"pv_done{t}", g[t] - 1)
+                    gg = g[t]
+
+                    def wait_pv(x):
+                        return ("wait", f"pv_done{t}{x & 1}", x >> 1)
+                    if not alias and gg > 0 and pv_wait_every_block:
+                        yield wait_pv(gg - 1)
                     if exchange_before_p:
                         store_p(t)
+                    if j > 0 and rnd.random() < rescale_prob:  # O rescale
+                        if alias and rescale_wait:
+                            yield wait_pv(gg - 1)
+                        assert o_done[t] >= gg - 1, f"tile {t}: O rescaled before P V({gg - 1}) is done"
+                    if alias and gg >= 2 and lag2_wait:
+                        yield wait_pv(gg - 2)
                     yield ("arrive", f"p_full{t}", 32)
                     g[t] += 1
             for t in range(2):
@@ -614,7 +643,8 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                 yield ("arrive", f"x{q}", 32)
                 yield ("wait", f"x{q}", xcount)
                 xcount += 1
-                yield ("wait", f"pv_done{t}", g[t] - 1)  # epilogue
+                yield ("wait", f"pv_done{t}{(g[t] - 1) & 1}", (g[t] - 1) >> 1)  # epilogue
+                assert o_done[t] == g[t] - 1, f"tile {t}: the epilogue reads O with P V done up to {o_done[t]}"
                 assert o_last[t] == g[t] - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]})"
         yield from take(len(items))
 
@@ -644,12 +674,15 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     for w in range(NW):
         agents[f"softmax{w}"] = softmax(w)
     waiting = {k: None for k in agents}
-    while agents or tensor_pipe or tma:
+    while agents or tensor_pipe or tma or late[0] or late[1]:
         ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
         if tensor_pipe:
             ready.append("#tensor")
         if tma:
             ready.append("#tma")
+        for t in range(2):
+            if late[t] and (rnd.random() < late_weight or not ready):
+                ready.append(f"#late{t}")
         if not ready:
             raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
         c = rnd.choice(ready)
@@ -657,8 +690,16 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
             op = tensor_pipe.pop(0)
             if op[0] == "mma":
                 execute(op[1], op[2], op[3])
+            elif op[0] == "late":
+                late[op[1]].append(op[2])
             else:
                 B[op[1]].arrive(1)
+            continue
+        if c.startswith("#late"):
+            t = int(c[-1])
+            gdone = late[t].pop(0)
+            o_done[t] = gdone
+            B[f"pv_done{t}{gdone & 1}"].arrive(1)
             continue
         if c == "#tma":
             B[tma.pop(rnd.randrange(len(tma)))].arrive(1)

@@ -132,6 +132,9 @@ def test_bk128_protocol_completes_without_hazards(N, causal, alias, rk, rv):
     for all_blocks in (False, True):
         for seed in range(4 if N <= 1000 else 2):
             assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, alias)
+            # P V commits that lag several products behind
+            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, alias, rescale_prob=0.3,
+                                  late_weight=0.05)
 
 
 def test_bk128_single_tile_units_and_packed_items():
@@ -188,6 +191,23 @@ def test_bk128_p_before_the_exchange_is_caught():
     for seed in range(20):
         try:
             simulate_bk128(1000, True, _items128(1000, True), 3, 2, seed, True, exchange_before_p=False)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
+
+
+@pytest.mark.parametrize("mutation", ["lag2_wait", "rescale_wait"])
+def test_bk128_d128_commit_waits_are_needed(mutation):
+    """d = 128 with P V commits arriving late: dropping the wait for P V(g-2) lets a
+    pv_done barrier run two phases ahead of a later wait, and dropping the wait
+    before a rescale lets O be rescaled while a product still adds to it: caught."""
+    from pipeline_model import simulate_bk128
+
+    caught = 0
+    for seed in range(30):
+        try:
+            simulate_bk128(2048, False, _items128(2048, True), 3, 2, seed, True, rescale_prob=0.3,
+                           late_weight=0.05, **{mutation: False})
         except AssertionError:
             caught += 1
     assert caught > 0
