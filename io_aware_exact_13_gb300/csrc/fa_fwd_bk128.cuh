@@ -26,24 +26,25 @@
 //            as soon as the softmax has copied S_t(j) to registers, so the
 //            softmax of block j+1 can start while P_t V_j runs.
 //
-// Softmax: both warpgroups work on one tile at a time. Warpgroup h takes keys
-// [64 h, 64 h + 64) of each 128-key block; thread r of each owns query row r
-// (TMEM lane r). The two halves of a row agree on the row maximum through
-// shared memory (warps q and q + 4 own the same 32 lanes and meet at a named
-// barrier), so both keep the same reference maximum; each keeps its own partial
-// denominator, and the two are added at the epilogue. The warpgroups take the
-// two tiles in turn: while they compute one tile's P, the tensor core runs the
-// other tile's P V and next S. (One warpgroup per tile, each thread doing all
-// 128 keys of its row, ran the two tiles' softmax passes side by side on the
-// same schedulers: about 2200 cycles per block each, twice the tile's tensor
-// time.)
+// Softmax: four warpgroups work on one tile at a time. Warpgroup h takes keys
+// [32 h, 32 h + 32) of each 128-key block; thread r of each owns query row r
+// (TMEM lane r). The four parts of a row agree on the row maximum through
+// shared memory (warps q, q + 4, q + 8, q + 12 own the same 32 lanes and meet at
+// an mbarrier), so all keep the same reference maximum; each keeps its own
+// partial denominator, and the four are added at the epilogue. The warpgroups
+// take the two tiles in turn: while they compute one tile's P, the tensor core
+// runs the other tile's P V and next S. Measured on the way here: one warpgroup
+// per tile doing all 128 keys of a row ran the two tiles' softmax side by side
+// (about 2200 cycles per block); two warpgroups per tile (64 keys each) spent
+// about 800 cycles in the exponent loop, which runs at 6.1 cycles per ex2
+// instruction with two warps per scheduler and 4.9 with four (the pipe's limit
+// is 4).
 //
-// Roles (16 warps, one persistent CTA per SM):
-//   warps 0-7   softmax + epilogue: warpgroup h = warp / 4 takes key half h
-//   warp  8     TMA producer: Q tiles per item, then K and V rings
-//   warps 9-10  issuer of tile t = warp - 9: S_t products and P_t V products
-//   warp  11    packed batch only: publishes the CTA's work items (ItemRing)
-//   warps 12-15 idle (they complete the last warpgroup)
+// Roles (20 warps, 640 threads, 96 registers each, one persistent CTA per SM):
+//   warps 0-15  softmax + epilogue: warpgroup h = warp / 4 takes key quarter h
+//   warp  16    TMA producer: Q tiles per item, then K and V rings
+//   warps 17-18 issuer of tile t = warp - 17: S_t products and P_t V products
+//   warp  19    packed batch only: publishes the CTA's work items (ItemRing)
 // Shared memory holds no static variables: the abort word, the item ring and
 // the row-maximum exchange live after the barriers in the dynamic region.
 #pragma once
@@ -52,7 +53,10 @@
 namespace fa {
 
 constexpr int kBK128 = 128;           // keys per K/V block
-constexpr int kItemConsumers128 = 11; // producer, two issuers, eight softmax warps
+constexpr int kThreads128 = 640;       // 20 warps
+constexpr int kSoftmaxWarps = 16;
+constexpr int kProducerWarp = 16;
+constexpr int kItemConsumers128 = 19;  // producer, two issuers, sixteen softmax warps
 constexpr int kStatusSmemAlign = -5;  // device status: the dynamic shared memory base was misaligned
 
 template <typename T, int D>
@@ -89,8 +93,8 @@ struct Cfg128 {
     static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 10 + 1;
     static constexpr int SMEM_TMEM_SLOT = SMEM_BAR + ((NUM_BARS * 8 + 15) / 16) * 16;
     static constexpr int SMEM_XBAR = SMEM_TMEM_SLOT + 16;         // 4 exchange barriers (one per lane quadrant)
-    static constexpr int SMEM_XCH = SMEM_XBAR + 32;               // float [2 parity][2 halves][128 rows]
-    static constexpr int SMEM_RING = SMEM_XCH + 2 * 2 * 128 * 4;  // ItemRing (packed batches)
+    static constexpr int SMEM_XCH = SMEM_XBAR + 32;               // float [4 quarters][128 rows]
+    static constexpr int SMEM_RING = SMEM_XCH + 4 * 128 * 4;      // ItemRing (packed batches)
     static constexpr int SMEM_ABORT = SMEM_RING + 128;
     static constexpr int SMEM_USED = SMEM_ABORT + 16;
     // up to 1024 bytes to align the base (SW128 tiles need 1024-byte alignment), within the 227 KB limit
@@ -124,7 +128,7 @@ struct Sync128 {
 };
 
 template <typename T, int D, bool CAUSAL, bool VARLEN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads128, 1)
     fa_fwd_bk128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using C = Cfg128<T, D>;
@@ -151,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.q_full(t), 1);
             mbar_init(sy.q_empty(t), 1);
             mbar_init(sy.s_full(t), 1);
-            mbar_init(sy.s_free(t), 2 * kBQ);  // both softmax warpgroups
-            mbar_init(sy.p_full(t), 2 * kBQ);
+            mbar_init(sy.s_free(t), 4 * kBQ);  // all four softmax warpgroups
+            mbar_init(sy.p_full(t), 4 * kBQ);
             mbar_init(sy.pv_done(t, 0), 1);
             mbar_init(sy.pv_done(t, 1), 1);
         }
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.v_empty(s), 2);
         }
         mbar_init(sy.drain(), 2);  // one commit per issuing warp
-        for (int q = 0; q < 4; ++q) mbar_init(smem_u32(xbar + q), 64);  // warps q and q + 4
+        for (int q = 0; q < 4; ++q) mbar_init(smem_u32(xbar + q), 128);  // warps q, q + 4, q + 8, q + 12
         if constexpr (VARLEN) {
             for (int i = 0; i < kItemRing; ++i) {
                 mbar_init(smem_u32(&ring->full[i]), 1);
@@ -176,11 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 9) {  // TMEM: all 512 columns (one CTA per SM)
+    if (warp == kProducerWarp + 1) {  // TMEM: all 512 columns (one CTA per SM)
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
@@ -190,9 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
-    if (warp >= 8) {
-        setmaxnreg_dec<64>();
-        if (warp == 8) {
+    if (warp >= kSoftmaxWarps) {
+        if (warp == kProducerWarp) {
             // ---------------------------------------------------------- TMA producer
             // Load order per item: Q tiles, K_0, then K_{j+1}, V_j for j = 0 .. nmax-1
             // (the order in which the issuers consume them).
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     while (!mbar_try_wait(sy.v_full(q % RV), (q / RV) & 1u) && global_timer_ns() - t0 < p.timeout_ns) {
                     }
             }
-        } else if (warp == 9 || warp == 10) {
+        } else if (warp == kProducerWarp + 1 || warp == kProducerWarp + 2) {
             // ---------------------------------------------------------- issuer of tile t
             // The whole warp runs the loop (warp-uniform), lane 0 issues.
             //   S_t(j)  = Q_t K_j^T     into S_t's columns, committed to s_full(t)
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // D = 128: P V(j) then S(j+1) (P_t lives in S_t's columns, in-order products).
             // D = 64:  S(j+1) as soon as the softmax has copied S(j) out, then P V(j).
             // K and V slots of blocks this tile does not need are released at once.
-            const int t = warp - 9;
+            const int t = warp - (kProducerWarp + 1);
             const uint32_t issue = lane == 0 ? 1u : 0u;
             const uint64_t a0 = smem_desc_sw128(smem_u32(smem + C::SMEM_Q + t * C::Q_TILE), 16, 1024);
             const uint64_t kd0 = smem_desc_sw128(smem_u32(smem + C::SMEM_K), 16, 1024);
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             tc_commit(sy.drain(), issue);
-        } else if (VARLEN && warp == 11) {
+        } else if (VARLEN && warp == kProducerWarp + 3) {
             // ---------------------------------------------------------- packed-batch item list
             VarlenCursor cur(p);
             bool more = true;
@@ -374,12 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        setmaxnreg_inc<192>();
         // -------------------------------------------------------------- softmax + epilogue
-        constexpr int HK = kBK128 / 2;  // keys per half
-        constexpr int HD = D / 2;       // O columns per half
-        const int h = warp >> 2;        // key half of this warpgroup
-        const int qd = warp & 3;        // TMEM lane quadrant (warps qd and qd + 4 share it)
+        constexpr int HK = kBK128 / 4;  // keys per quarter
+        constexpr int HD = D / 4;       // O columns per quarter
+        const int h = warp >> 2;        // key quarter of this warpgroup
+        const int qd = warp & 3;        // TMEM lane quadrant (warps qd, qd + 4, qd + 8, qd + 12 share it)
         const int r = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const float scale_log2 = p.scale_log2;
@@ -388,21 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         // non-positive scale is not -inf)
         const bool fast = scale_log2 > 0.0f;
         const float sl2 = fast ? scale_log2 : 1.0f;
-        uint32_t xcount = 0;  // exchanges with the partner thread (phase of the pair's barrier)
-        // The partner (same row, other key half) receives v; returns the partner's value. The
-        // pair meets at an mbarrier with the same bounded wait as every pipeline wait (a warp
-        // that gives up does not leave its partner waiting forever). Buffers alternate by
-        // phase: a value is overwritten two exchanges later, after the partner has read it.
-        const uint32_t pair_bar = smem_u32(xbar + qd);
-        auto exchange = [&](float v, bool &okx) -> float {
-            float *buf = xch + (xcount & 1u) * 256;
-            buf[h * 128 + r] = v;
-            tc_fence_before();  // this thread's tensor-memory reads come before the partner's writes
-            mbar_arrive(pair_bar);
-            okx = wait_warp(pair_bar, xcount & 1u, abort_flag, p);
-            ++xcount;
+        // The four parts of a row (same row, other key quarters) exchange one value each at the
+        // quadrant's mbarrier, with the same bounded wait as every pipeline wait (a warp that gives
+        // up does not leave the others waiting forever). Each exchange takes two phases: all four
+        // write and arrive (even phase), read the other three, and arrive again (odd phase); the
+        // next exchange writes only after the odd phase, so one buffer suffices.
+        uint32_t xk = 0;
+        const uint32_t quad_bar = smem_u32(xbar + qd);
+        auto exchange = [&](float v, bool &okx, float &o1, float &o2, float &o3) {
+            if (xk > 0) {
+                okx = wait_warp(quad_bar, 1u, abort_flag, p);  // the previous values have been read
+                if (!okx) return;
+            }
+            xch[h * 128 + r] = v;
+            tc_fence_before();  // this thread's tensor-memory reads come before the others' writes
+            mbar_arrive(quad_bar);
+            okx = wait_warp(quad_bar, 0u, abort_flag, p);
+            if (!okx) return;
             tc_fence_after();
-            return buf[(h ^ 1) * 128 + r];
+            o1 = xch[((h + 1) & 3) * 128 + r];
+            o2 = xch[((h + 2) & 3) * 128 + r];
+            o3 = xch[((h + 3) & 3) * 128 + r];
+            mbar_arrive(quad_bar);
+            ++xk;
         };
         uint32_t scount[2] = {0, 0};  // S blocks consumed per tile (all items)
         uint32_t g[2] = {0, 0};       // P blocks produced per tile = its P V products
@@ -417,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (!ok || j >= nt[t]) continue;
-                    const uint32_t s_addr = tmem + lane_base + 128 * t + HK * h;  // fp32 S columns of this half
+                    const uint32_t s_addr = tmem + lane_base + 128 * t + HK * h;  // fp32 S columns of this quarter
                     const uint32_t p_addr = tmem + lane_base + C::TM_P + C::TM_P_STRIDE * t + HK / 2 * h;
                     const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t + HD * h;
                     ok = wait_warp(sy.s_full(t), scount[t] & 1u, abort_flag, p);
@@ -427,8 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float x[HK];
                     {
                         uint32_t sr[HK];
-                        tmem_ld64_nowait(s_addr, sr);
-                        tmem_wait_ld_dep64(sr);
+                        tmem_ld32_wait(s_addr, sr);
 #pragma unroll
                         for (int c = 0; c < HK; ++c)
                             x[c] = fast ? __uint_as_float(sr[c]) : __uint_as_float(sr[c]) * scale_log2;
@@ -452,16 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[24 + i], x[32 + i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[40 + i], x[48 + i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[56 + i]);
-                    const float mhalf =
+                    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[24 + i]);
+                    const float mq =
                         fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                    const float mother = exchange(mhalf, ok);
+                    float mo1, mo2, mo3;
+                    exchange(mq, ok, mo1, mo2, mo3);
                     if (!ok) break;
-                    const float mb = fmaxf(mhalf, mother) * sl2;  // sl2 > 0
+                    const float mb = fmaxf(mq, fmax3(mo1, mo2, mo3)) * sl2;  // sl2 > 0
                     const float m_new = fmaxf(m_ref[t], mb);
                     // lazy rescale: move the reference only when the maximum grew by more than TAU
                     const bool need = (m_new > m_ref[t] + kTau) || (m_ref[t] == -INFINITY && m_new != -INFINITY);
@@ -491,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     //  D = 128: before rescaling O. P(g) goes over S(g)'s columns, which the tensor
                     //           core wrote after P V(g-1) had read P(g-1) there (it runs one issuing
                     //           thread's products in order), and the softmax stores only after it
-                    //           has seen S(g) complete. (The P of the second key half lands on S
-                    //           columns of the first half, which the partner copied out before the
+                    //           has seen S(g) complete. (The P of key quarter h lands on S columns
+                    //           [16 h, 16 h + 16), which quarters 0 and 1 copied out before the
                     //           exchange.)
                     // Besides, P V(g-2) (long complete) is waited for before P(g) is released, so
                     // that neither pv_done barrier can get two phases ahead of these waits.
@@ -504,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    tmem_st32(p_addr, pv);
+                    tmem_st16(p_addr, pv);
                     if (rescale) {
                         if (C::ALIAS) {
                             ok = wait_pv(g[t] - 1);
@@ -514,12 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // O holds P V for blocks < j relative to the old reference: scale this half's
                         // columns of the row (alpha = 1 where the reference did not move)
 #pragma unroll
-                        for (int c0 = 0; c0 < HD; c0 += 32) {
-                            uint32_t ov[32];
-                            tmem_ld32_wait(o_addr + c0, ov);
+                        for (int c0 = 0; c0 < HD; c0 += 16) {
+                            uint32_t ov[16];
+                            tmem_ld16_wait(o_addr + c0, ov);
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                            tmem_st32(o_addr + c0, ov);
+                            for (int c = 0; c < 16; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                            tmem_st16(o_addr + c0, ov);
                         }
                     }
                     if (C::ALIAS && g[t] >= 2) {
@@ -537,9 +543,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (!ok || nt[t] == 0) continue;
-                const float l_other = exchange(l[t], ok);  // the other half's partial denominator
+                float lo1, lo2, lo3;
+                exchange(l[t], ok, lo1, lo2, lo3);  // the other quarters' partial denominators
                 if (!ok) break;
-                const float l_row = l[t] + l_other;
+                const float l_row = (l[t] + lo1) + (lo2 + lo3);
                 ok = wait_warp(sy.pv_done(t, (g[t] - 1) & 1u), ((g[t] - 1) >> 1) & 1u, abort_flag, p);
                 if (!ok) break;
                 tc_fence_after();
@@ -550,12 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                : ((size_t)bh * p.N + (size_t)row);
                 T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D + HD * h;
 #pragma unroll
-                for (int c0 = 0; c0 < HD; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32_wait(o_addr + c0, ov);
+                for (int c0 = 0; c0 < HD; c0 += 16) {
+                    uint32_t ov[16];
+                    tmem_ld16_wait(o_addr + c0, ov);
                     if (row < n) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 8)
+                        for (int c = 0; c < 16; c += 8)
                             st_global_v4(orow + c0 + c,
                                          pack2<T>(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv),
                                          pack2<T>(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv),
@@ -574,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kProducerWarp + 1) {
         // every MMA of both issuing warps must be complete before TMEM is released
         const uint64_t t0 = global_timer_ns();
         while (!mbar_try_wait(sy.drain(), 0) && global_timer_ns() - t0 < p.timeout_ns) {

@@ -259,6 +259,17 @@ __device__ __forceinline__ void tmem_wait_ld_dep64(uint32_t (&r)[64]) {
                  : "memory");
 }
 
+// Each thread reads 16 consecutive 32-bit columns of its own lane, then waits.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : FA_R8(0), FA_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+
 // Each thread writes 32 consecutive 32-bit columns of its own lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(

@@ -421,16 +421,18 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     one issuing warp per query tile (S_t and P_t V products), the eight softmax
     warps and (``item_ring`` > 0) the packed-batch item list.
 
-    The softmax warps work on one tile at a time: warp w = 4 h + q takes key half h
-    of TMEM lane quadrant q, for tile 0 then tile 1 of each block; warps q and
-    q + 4 (the same rows) exchange their row maxima at a pair barrier before
-    computing P, and their partial denominators at the epilogue.
+    The sixteen softmax warps work on one tile at a time: warp w = 4 h + q takes
+    key quarter h of TMEM lane quadrant q, for tile 0 then tile 1 of each block;
+    warps q, q + 4, q + 8, q + 12 (the same rows) exchange their row maxima at the
+    quadrant's barrier before computing P, and their partial denominators at the
+    epilogue (each exchange: write and arrive, wait for the even phase, read,
+    arrive; the next write waits for the odd phase).
 
     ``alias`` is the d = 128 layout, where P_t is written over S_t's tensor-memory
-    columns (key half h of P over S columns [32 h, 32 h + 32), which belong to
-    half 0): the issuer orders O += P V(j) before S(j+1). Besides the barrier
-    checks of ``simulate`` this model tracks what each 32-column quarter of each
-    lane quadrant holds, so that a product that overwrites P before the P V
+    columns (key quarter h of P over S columns [16 h, 16 h + 16), which belong to
+    quarters 0 and 1): the issuer orders O += P V(j) before S(j+1). Besides the
+    barrier checks of ``simulate`` this model tracks what each 16-column unit of
+    each lane quadrant holds, so that a product that overwrites P before the P V
     product has read it, a P written over S columns that their owner has not
     copied out, or a softmax that reads S before it is complete, fails here.
     The commits of P V products (to pv_done(t, g & 1)) may reach their barriers
@@ -444,21 +446,21 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     Mutations that must be caught: ``in_order_pv_then_s=False`` (an aliasing
     issuer that issues S(j+1) before P V(j)), ``pv_wait_every_block=False`` (at
     d = 64, a softmax that stores P(j) before P V(j-1) has read its buffer),
-    ``exchange_before_p=False`` (half 1 writes its P before the pair exchange,
-    over S columns half 0 may not have copied out), ``lag2_wait=False`` (d = 128
+    ``exchange_before_p=False`` (a quarter writes its P before the exchange, over
+    S columns another quarter may not have copied out), ``lag2_wait=False`` (d = 128
     without the wait for P V(g-2): a barrier runs two phases ahead of a later
     wait), ``rescale_wait=False`` (d = 128, O rescaled without waiting for
     P V(g-1))."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
-    NW = 8
+    NW = 16
 
     def bar(name, count):
         B[name] = Bar(name, count)
 
     for t in range(2):
-        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", 2 * BQ), ("p_full", 2 * BQ),
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", 4 * BQ), ("p_full", 4 * BQ),
                         ("pv_done0", 1), ("pv_done1", 1)):
             bar(f"{name}{t}", c)
     for s_ in range(rk):
@@ -468,7 +470,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
         bar(f"v_full{s_}", 1)
         bar(f"v_empty{s_}", 2)
     for q in range(4):
-        bar(f"x{q}", 64)
+        bar(f"x{q}", 128)
     consumers = 3 + NW
     for s_ in range(item_ring):
         bar(f"item_full{s_}", 1)
@@ -476,10 +478,11 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     tensor_pipe, tma = [], []
     late = [[], []]          # per tile: P V commits executed but not yet arrived (in order)
     o_done = [-1, -1]        # per tile: the last P V product whose commit has arrived
-    # per tile, lane quadrant and 32-column quarter of S_t: ("S", g, owner_has_read) or ("P", g)
-    scols = [[[None] * 4 for _ in range(4)] for _ in range(2)]
-    pbuf = [[[None] * 2 for _ in range(4)] for _ in range(2)]  # d = 64: P_t's own buffer, per half
+    # per tile, lane quadrant and 16-column unit of S_t: ("S", g, owner_has_read) or ("P", g)
+    scols = [[[None] * 8 for _ in range(4)] for _ in range(2)]
+    pbuf = [[[None] * 4 for _ in range(4)] for _ in range(2)]  # d = 64: P_t's own buffer, per quarter
     sread_count = [{}, {}]   # S block -> quarters copied out
+    xbuf = [[(-1, None)] * 4 for _ in range(4)]  # per lane quadrant: the value each quarter wrote last
     pv_read = [set(), set()]
     o_last = [None, None]
 
@@ -586,10 +589,23 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
 
     def softmax(w):
         h, q = w // 4, w % 4
-        scount, g, xcount = [0, 0], [0, 0], 0
+        scount, g = [0, 0], [0, 0]
+        xk = [0]
+
+        def exchange():
+            k = xk[0]
+            if k > 0:
+                yield ("wait", f"x{q}", 2 * k - 1)  # the previous values have been read
+            xbuf[q][h] = (k, w)
+            yield ("arrive", f"x{q}", 32)
+            yield ("wait", f"x{q}", 2 * k)
+            for o in range(4):
+                assert xbuf[q][o][0] == k, f"quadrant {q}: exchange {k} reads {xbuf[q][o]} from quarter {o}"
+            yield ("arrive", f"x{q}", 32)
+            xk[0] += 1
 
         def store_p(t):
-            if alias:  # half h of P over quarter h, owned by half 0
+            if alias:  # quarter h of P over unit h (S keys [16 h, 16 h + 16), owned by quarter h // 2)
                 cell = scols[t][q][h]
                 assert cell is not None and cell[0] == "S" and cell[1] == g[t] and cell[2], (
                     f"tile {t}: P({g[t]}) half {h} written over {cell} (not yet copied out)")
@@ -609,7 +625,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                         continue
                     yield ("wait", f"s_full{t}", scount[t])
                     scount[t] += 1
-                    for c in (2 * h, 2 * h + 1):
+                    for c in (2 * h, 2 * h + 1):  # units of S keys [32 h, 32 h + 32)
                         cell = scols[t][q][c]
                         assert cell is not None and cell[:2] == ("S", g[t]), (
                             f"tile {t}: softmax reads S({g[t]}) but quarter {c} holds {cell}")
@@ -618,9 +634,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                         yield ("arrive", f"s_free{t}", 32)
                     if not exchange_before_p:
                         store_p(t)
-                    yield ("arrive", f"x{q}", 32)
-                    yield ("wait", f"x{q}", xcount)
-                    xcount += 1
+                    yield from exchange()
                     gg = g[t]
 
                     def wait_pv(x):
@@ -640,9 +654,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
             for t in range(2):
                 if not n[t]:
                     continue
-                yield ("arrive", f"x{q}", 32)
-                yield ("wait", f"x{q}", xcount)
-                xcount += 1
+                yield from exchange()
                 yield ("wait", f"pv_done{t}{(g[t] - 1) & 1}", (g[t] - 1) >> 1)  # epilogue
                 assert o_done[t] == g[t] - 1, f"tile {t}: the epilogue reads O with P V done up to {o_done[t]}"
                 assert o_last[t] == g[t] - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]})"
@@ -651,7 +663,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
     def execute(kind, t, g):
         if kind == "S":
             for q in range(4):
-                for c in range(4):
+                for c in range(8):
                     prev = scols[t][q][c]
                     if prev is None:
                         continue
@@ -659,10 +671,10 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                         assert prev[1] in pv_read[t], f"tile {t}: S({g}) overwrites {prev} before its P V read it"
                     else:
                         assert len(prev) == 3 and prev[2], f"tile {t}: S({g}) overwrites S{prev} before it was read"
-            scols[t] = [[("S", g, False)] * 4 for _ in range(4)]
+            scols[t] = [[("S", g, False)] * 8 for _ in range(4)]
         else:
             for q in range(4):
-                held = scols[t][q][:2] if alias else pbuf[t][q]
+                held = scols[t][q][:4] if alias else pbuf[t][q]
                 for cell in held:
                     assert cell == ("P", g), f"tile {t}: P V({g}) reads {cell}"
             pv_read[t].add(g)

@@ -206,8 +206,9 @@ def test_bk128_d128_commit_waits_are_needed(mutation):
     caught = 0
     for seed in range(30):
         try:
-            simulate_bk128(2048, False, _items128(2048, True), 3, 2, seed, True, rescale_prob=0.3,
-                           late_weight=0.05, **{mutation: False})
+            simulate_bk128(2048, False, _items128(2048, True), 3, 2, seed, True,
+                           rescale_prob=0.0 if mutation == "lag2_wait" else 0.3, late_weight=0.05,
+                           **{mutation: False})
         except AssertionError:
             caught += 1
     assert caught > 0
