@@ -100,10 +100,11 @@ template <typename T, int D, bool CAUSAL, bool VARLEN>
 int launch_bk128(const LaunchArgs &a) {
     using C = Cfg128<T, D>;
     auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN>;
-    // 640 threads, one CTA per SM: at most 65536 / 640 registers per thread.
+    // The register split between warpgroups assumes 128 registers per thread at
+    // launch (512 x 128 = 256 x 192 + 256 x 64). Refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
-    if (attr.numRegs * kThreads128 > 65536) return -5;
+    if (attr.numRegs * kThreads < 256 * 192 + 256 * 64) return -5;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return -5;
     CUtensorMap tq, tk, tv;
@@ -140,7 +141,7 @@ int launch_bk128(const LaunchArgs &a) {
     p.Hkv = a.Hkv;
     p.mask_tma = 0;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    kern<<<grid, kThreads128, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

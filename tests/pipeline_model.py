@@ -414,77 +414,66 @@ def simulate_bwd_halves(n_it, stages, seed):
     return True
 
 
-def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item_ring=0,
-                   in_order_pv_then_s=True, pv_wait_every_block=True, exchange_before_p=True,
-                   lag2_wait=True, rescale_wait=True, late_weight=1.0):
+def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0, s_waits_free=True,
+                   p_waits_pv=True, late_weight=1.0, one_exchange_buffer=False):
     """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
-    one issuing warp per query tile (S_t and P_t V products), the eight softmax
-    warps and (``item_ring`` > 0) the packed-batch item list.
+    the S issuer (S_t(j) for t = 0, 1 in turn into the one S buffer), one P V
+    issuer per tile, the eight softmax warps and (``item_ring`` > 0) the
+    packed-batch item list.
 
-    The sixteen softmax warps work on one tile at a time: warp w = 4 h + q takes
-    key quarter h of TMEM lane quadrant q, for tile 0 then tile 1 of each block;
-    warps q, q + 4, q + 8, q + 12 (the same rows) exchange their row maxima at the
-    quadrant's barrier before computing P, and their partial denominators at the
-    epilogue (each exchange: write and arrive, wait for the even phase, read,
-    arrive; the next write waits for the odd phase).
+    The softmax warps take the S products in issue order: warp w = 4 h + q takes
+    key half h of TMEM lane quadrant q; warps q and q + 4 (the same rows) exchange
+    their row maxima at the pair barrier x{q} before computing P (buffers by
+    exchange parity), and their partial denominators at the epilogue.
 
-    ``alias`` is the d = 128 layout, where P_t is written over S_t's tensor-memory
-    columns (key quarter h of P over S columns [16 h, 16 h + 16), which belong to
-    quarters 0 and 1): the issuer orders O += P V(j) before S(j+1). Besides the
-    barrier checks of ``simulate`` this model tracks what each 16-column unit of
-    each lane quadrant holds, so that a product that overwrites P before the P V
-    product has read it, a P written over S columns that their owner has not
-    copied out, or a softmax that reads S before it is complete, fails here.
-    The commits of P V products (to pv_done(t, g & 1)) may reach their barriers
-    late, after the commits of products issued after them (measured on the GPU:
-    several hundred cycles after the next S), but in order among themselves
-    (``late_weight`` < 1 makes the scheduler deliver them rarely, so that they lag
-    by several products); a P V
-    product's accumulation into O counts as done only when its commit arrives, and
-    the softmax may rescale or read O only after every earlier product is done.
+    Besides the barrier checks of ``simulate`` the model tracks the S buffer and
+    each tile's P buffer, so that an S product that overwrites an S the softmax
+    has not copied out, a P stored over one its P V product has not read, or a
+    softmax that reads the wrong S, fails here. The commits of P V products may
+    reach their barriers late (measured on the GPU: several hundred cycles after
+    later commits), in order among themselves (``late_weight`` < 1 delays them
+    further); a P V product counts as done for O only when its commit arrives,
+    and the softmax may rescale or read O only after all earlier ones are done.
 
-    Mutations that must be caught: ``in_order_pv_then_s=False`` (an aliasing
-    issuer that issues S(j+1) before P V(j)), ``pv_wait_every_block=False`` (at
-    d = 64, a softmax that stores P(j) before P V(j-1) has read its buffer),
-    ``exchange_before_p=False`` (a quarter writes its P before the exchange, over
-    S columns another quarter may not have copied out), ``lag2_wait=False`` (d = 128
-    without the wait for P V(g-2): a barrier runs two phases ahead of a later
-    wait), ``rescale_wait=False`` (d = 128, O rescaled without waiting for
-    P V(g-1))."""
+    Mutations that must be caught: ``s_waits_free=False`` (the S issuer does not
+    wait for the S buffer to be copied out), ``p_waits_pv=False`` (the softmax
+    stores P_t(g) without waiting for P V_t(g-1), and rescales O without it),
+    ``one_exchange_buffer=True`` (one exchange buffer instead of one per parity:
+    a fast pair member overwrites a value its partner has not read)."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
-    NW = 16
+    NW = 8
 
     def bar(name, count):
         B[name] = Bar(name, count)
 
     for t in range(2):
-        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("s_free", 4 * BQ), ("p_full", 4 * BQ),
-                        ("pv_done0", 1), ("pv_done1", 1)):
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("p_full", 2 * BQ), ("pv_done0", 1),
+                        ("pv_done1", 1)):
             bar(f"{name}{t}", c)
+    bar("s_free", 2 * BQ)
     for s_ in range(rk):
         bar(f"k_full{s_}", 1)
-        bar(f"k_empty{s_}", 2)
+        bar(f"k_empty{s_}", 1)
     for s_ in range(rv):
         bar(f"v_full{s_}", 1)
         bar(f"v_empty{s_}", 2)
     for q in range(4):
-        bar(f"x{q}", 128)
-    consumers = 3 + NW
+        bar(f"x{q}", 64)
+    consumers = 4 + NW
     for s_ in range(item_ring):
         bar(f"item_full{s_}", 1)
         bar(f"item_empty{s_}", consumers)
     tensor_pipe, tma = [], []
     late = [[], []]          # per tile: P V commits executed but not yet arrived (in order)
     o_done = [-1, -1]        # per tile: the last P V product whose commit has arrived
-    # per tile, lane quadrant and 16-column unit of S_t: ("S", g, owner_has_read) or ("P", g)
-    scols = [[[None] * 8 for _ in range(4)] for _ in range(2)]
-    pbuf = [[[None] * 4 for _ in range(4)] for _ in range(2)]  # d = 64: P_t's own buffer, per quarter
-    sread_count = [{}, {}]   # S block -> quarters copied out
-    xbuf = [[(-1, None)] * 4 for _ in range(4)]  # per lane quadrant: the value each quarter wrote last
+    o_last = [None, None]    # per tile: the last P V product executed
+    sbuf = [None]            # the S buffer: (tile, block index of the tile)
+    sreads = {}              # (tile, g) -> softmax warps that copied it out
+    pbuf = [[[None] * 2 for _ in range(4)] for _ in range(2)]  # per tile, quadrant, half: ("P", g)
     pv_read = [set(), set()]
-    o_last = [None, None]
+    xbuf = [[[(-1, None)] * 2 for _ in range(2)] for _ in range(4)]  # [quadrant][parity][half]
 
     def nkv(n_seq, q0, t):
         r0 = q0 + t * BQ
@@ -537,54 +526,48 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                     vpos += 1
         yield from take(len(items))
 
-    def issuer(t):
-        st = {"q": 0, "k": 0, "v": 0, "p": 0, "s": 0}
-
-        def issue_s(j, nt, gidx):
-            s_ = st["k"] % rk
-            yield ("wait", f"k_full{s_}", st["k"] // rk)
-            st["k"] += 1
-            if j >= nt:
-                yield ("arrive", f"k_empty{s_}", 1)
-                return
-            if not alias and st["s"] > 0:
-                yield ("wait", f"s_free{t}", st["s"] - 1)
-            st["s"] += 1
-            tensor_pipe.extend([("mma", "S", t, gidx), ("commit", f"s_full{t}")]
-                               + ([("commit", f"q_empty{t}")] if j == nt - 1 else []) + [("commit", f"k_empty{s_}")])
-
-        def issue_pv(j, nt, gidx):
-            s_ = st["v"] % rv
-            yield ("wait", f"v_full{s_}", st["v"] // rv)
-            st["v"] += 1
-            if j >= nt:
-                yield ("arrive", f"v_empty{s_}", 1)
-                return
-            yield ("wait", f"p_full{t}", st["p"])
-            st["p"] += 1
-            tensor_pipe.extend([("mma", "PV", t, gidx), ("late", t, gidx), ("commit", f"v_empty{s_}")])
-
-        g0 = 0
+    def s_issuer():
+        qcount, kpos, issued = [0, 0], 0, 0
+        g0 = [0, 0]
         for i, q0 in enumerate(items):
             yield from take(i)
             n, nmax = counts(q0)
-            nt = n[t]
-            if nmax == 0:
-                continue
-            if nt:
-                yield ("wait", f"q_full{t}", st["q"])
-                st["q"] += 1
-            yield from issue_s(0, nt, g0)
+            for t in range(2):
+                if n[t]:
+                    yield ("wait", f"q_full{t}", qcount[t])
+                    qcount[t] += 1
             for j in range(nmax):
-                if alias and in_order_pv_then_s:
-                    yield from issue_pv(j, nt, g0 + j)
-                    if j + 1 < nmax:
-                        yield from issue_s(j + 1, nt, g0 + j + 1)
-                else:
-                    if j + 1 < nmax:
-                        yield from issue_s(j + 1, nt, g0 + j + 1)
-                    yield from issue_pv(j, nt, g0 + j)
-            g0 += nt
+                s_ = kpos % rk
+                yield ("wait", f"k_full{s_}", kpos // rk)
+                kpos += 1
+                for t in range(2):
+                    if j >= n[t]:
+                        continue
+                    if issued and s_waits_free:
+                        yield ("wait", "s_free", issued - 1)
+                    issued += 1
+                    tensor_pipe.extend([("mma", "S", t, g0[t] + j), ("commit", f"s_full{t}")]
+                                       + ([("commit", f"q_empty{t}")] if j == n[t] - 1 else []))
+                tensor_pipe.append(("commit", f"k_empty{s_}"))
+            for t in range(2):
+                g0[t] += n[t]
+        yield from take(len(items))
+
+    def pv_issuer(t):
+        vpos = pcount = 0
+        for i, q0 in enumerate(items):
+            yield from take(i)
+            n, nmax = counts(q0)
+            for j in range(nmax):
+                s_ = vpos % rv
+                yield ("wait", f"v_full{s_}", vpos // rv)
+                vpos += 1
+                if j >= n[t]:
+                    yield ("arrive", f"v_empty{s_}", 1)
+                    continue
+                yield ("wait", f"p_full{t}", pcount)
+                tensor_pipe.extend([("mma", "PV", t, pcount), ("late", t, pcount), ("commit", f"v_empty{s_}")])
+                pcount += 1
         yield from take(len(items))
 
     def softmax(w):
@@ -594,27 +577,13 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
 
         def exchange():
             k = xk[0]
-            if k > 0:
-                yield ("wait", f"x{q}", 2 * k - 1)  # the previous values have been read
-            xbuf[q][h] = (k, w)
+            par = 0 if one_exchange_buffer else k & 1
+            xbuf[q][par][h] = (k, w)
             yield ("arrive", f"x{q}", 32)
-            yield ("wait", f"x{q}", 2 * k)
-            for o in range(4):
-                assert xbuf[q][o][0] == k, f"quadrant {q}: exchange {k} reads {xbuf[q][o]} from quarter {o}"
-            yield ("arrive", f"x{q}", 32)
+            yield ("wait", f"x{q}", k)
+            other = xbuf[q][par][1 - h]
+            assert other[0] == k, f"quadrant {q}: exchange {k} reads {other} from the other half"
             xk[0] += 1
-
-        def store_p(t):
-            if alias:  # quarter h of P over unit h (S keys [16 h, 16 h + 16), owned by quarter h // 2)
-                cell = scols[t][q][h]
-                assert cell is not None and cell[0] == "S" and cell[1] == g[t] and cell[2], (
-                    f"tile {t}: P({g[t]}) half {h} written over {cell} (not yet copied out)")
-                scols[t][q][h] = ("P", g[t])
-            else:
-                cell = pbuf[t][q][h]
-                assert cell is None or cell[1] in pv_read[t], (
-                    f"tile {t}: P({g[t]}) overwrites P{cell} before its P V product read it")
-                pbuf[t][q][h] = ("P", g[t])
 
         for i, q0 in enumerate(items):
             yield from take(i)
@@ -625,30 +594,18 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
                         continue
                     yield ("wait", f"s_full{t}", scount[t])
                     scount[t] += 1
-                    for c in (2 * h, 2 * h + 1):  # units of S keys [32 h, 32 h + 32)
-                        cell = scols[t][q][c]
-                        assert cell is not None and cell[:2] == ("S", g[t]), (
-                            f"tile {t}: softmax reads S({g[t]}) but quarter {c} holds {cell}")
-                        scols[t][q][c] = ("S", g[t], True)
-                    if not alias:
-                        yield ("arrive", f"s_free{t}", 32)
-                    if not exchange_before_p:
-                        store_p(t)
+                    assert sbuf[0] == (t, g[t]), f"softmax {w} expects S({t}, {g[t]}) but the buffer holds {sbuf[0]}"
+                    sreads[(t, g[t])] = sreads.get((t, g[t]), 0) + 1
+                    yield ("arrive", "s_free", 32)
                     yield from exchange()
-                    gg = g[t]
-
-                    def wait_pv(x):
-                        return ("wait", f"pv_done{t}{x & 1}", x >> 1)
-                    if not alias and gg > 0 and pv_wait_every_block:
-                        yield wait_pv(gg - 1)
-                    if exchange_before_p:
-                        store_p(t)
-                    if j > 0 and rnd.random() < rescale_prob:  # O rescale
-                        if alias and rescale_wait:
-                            yield wait_pv(gg - 1)
-                        assert o_done[t] >= gg - 1, f"tile {t}: O rescaled before P V({gg - 1}) is done"
-                    if alias and gg >= 2 and lag2_wait:
-                        yield wait_pv(gg - 2)
+                    if g[t] > 0 and p_waits_pv:
+                        yield ("wait", f"pv_done{t}{(g[t] - 1) & 1}", (g[t] - 1) >> 1)
+                    cell = pbuf[t][q][h]
+                    assert cell is None or cell[1] in pv_read[t], (
+                        f"tile {t}: P({g[t]}) overwrites P{cell} before its P V product read it")
+                    pbuf[t][q][h] = ("P", g[t])
+                    if j > 0 and rnd.random() < rescale_prob:
+                        assert o_done[t] >= g[t] - 1, f"tile {t}: O rescaled before P V({g[t] - 1}) is done"
                     yield ("arrive", f"p_full{t}", 32)
                     g[t] += 1
             for t in range(2):
@@ -662,25 +619,18 @@ def simulate_bk128(N, causal, items, rk, rv, seed, alias, rescale_prob=0.1, item
 
     def execute(kind, t, g):
         if kind == "S":
-            for q in range(4):
-                for c in range(8):
-                    prev = scols[t][q][c]
-                    if prev is None:
-                        continue
-                    if prev[0] == "P":
-                        assert prev[1] in pv_read[t], f"tile {t}: S({g}) overwrites {prev} before its P V read it"
-                    else:
-                        assert len(prev) == 3 and prev[2], f"tile {t}: S({g}) overwrites S{prev} before it was read"
-            scols[t] = [[("S", g, False)] * 8 for _ in range(4)]
+            prev = sbuf[0]
+            assert prev is None or sreads.get(prev, 0) == NW, (
+                f"S({t}, {g}) overwrites S{prev} copied out by {sreads.get(prev, 0)} of {NW} warps")
+            sbuf[0] = (t, g)
         else:
             for q in range(4):
-                held = scols[t][q][:4] if alias else pbuf[t][q]
-                for cell in held:
+                for cell in pbuf[t][q]:
                     assert cell == ("P", g), f"tile {t}: P V({g}) reads {cell}"
             pv_read[t].add(g)
             o_last[t] = g
 
-    agents = {"producer": producer(), "I0": issuer(0), "I1": issuer(1)}
+    agents = {"producer": producer(), "S": s_issuer(), "PV0": pv_issuer(0), "PV1": pv_issuer(1)}
     if item_ring:
         agents["scheduler"] = scheduler()
     for w in range(NW):

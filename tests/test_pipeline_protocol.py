@@ -125,15 +125,15 @@ def _items128(N, all_blocks):
 
 @pytest.mark.parametrize("N,causal", [(1000, True), (4096, True), (384, True), (200, True), (129, False),
                                       (1000, False), (64, False), (1, True), (256, True), (257, False)])
-@pytest.mark.parametrize("alias,rk,rv", [(True, 3, 2), (False, 6, 6), (True, 2, 2)])
-def test_bk128_protocol_completes_without_hazards(N, causal, alias, rk, rv):
+@pytest.mark.parametrize("rk,rv", [(3, 2), (6, 6), (2, 2)])
+def test_bk128_protocol_completes_without_hazards(N, causal, rk, rv):
     from pipeline_model import simulate_bk128
 
     for all_blocks in (False, True):
         for seed in range(4 if N <= 1000 else 2):
-            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, alias)
+            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed)
             # P V commits that lag several products behind
-            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, alias, rescale_prob=0.3,
+            assert simulate_bk128(N, causal, _items128(N, all_blocks), rk, rv, seed, rescale_prob=0.3,
                                   late_weight=0.05)
 
 
@@ -146,69 +146,25 @@ def test_bk128_single_tile_units_and_packed_items():
     n_items = (max(lengths) + ROWS - 1) // ROWS
     packed = [(qb * ROWS, L) for qb in range(n_items - 1, -1, -1) for L in lengths]
     single = [(512, 1000, 640), (512, 1000, 1000), (768, 1000, 896), (0, 1000, 128)]
-    for alias in (True, False):
-        for seed in range(4):
-            assert simulate_bk128(max(lengths), True, packed, 3, 2, seed, alias, item_ring=4)
-            assert simulate_bk128(max(lengths), False, packed, 6, 6, seed, alias, item_ring=4)
-            assert simulate_bk128(1000, True, single, 3, 2, seed, alias)
+    for seed in range(4):
+        assert simulate_bk128(max(lengths), True, packed, 3, 2, seed, item_ring=4)
+        assert simulate_bk128(max(lengths), False, packed, 6, 6, seed, item_ring=4)
+        assert simulate_bk128(1000, True, single, 3, 2, seed)
 
 
-def test_bk128_overwriting_p_before_its_product_is_caught():
-    """An aliasing issuer that issues S(j+1) before P V(j) overwrites P: caught."""
-    from pipeline_model import simulate_bk128
-
-    caught = 0
-    for seed in range(10):
-        try:
-            simulate_bk128(1000, True, _items128(1000, True), 3, 2, seed, True, in_order_pv_then_s=False)
-        except AssertionError:
-            caught += 1
-    assert caught > 0
-
-
-def test_bk128_skipping_the_per_block_commit_wait_is_caught():
-    """d = 64 (P_t in its own buffer): a softmax that stores P(j) without waiting
-    for the commit of P V(j-1) overwrites a P that the tensor core has not read
-    yet: caught."""
-    from pipeline_model import simulate_bk128
-
-    caught = 0
-    for seed in range(20):
-        try:
-            simulate_bk128(2048, False, _items128(2048, True), 6, 6, seed, False, pv_wait_every_block=False,
-                           rescale_prob=0.0)
-        except AssertionError:
-            caught += 1
-    assert caught > 0
-
-
-def test_bk128_p_before_the_exchange_is_caught():
-    """d = 128: the second key half's P lands on S columns of the first half; writing
-    it before the pair exchange (before the first half has copied them out): caught."""
-    from pipeline_model import simulate_bk128
-
-    caught = 0
-    for seed in range(20):
-        try:
-            simulate_bk128(1000, True, _items128(1000, True), 3, 2, seed, True, exchange_before_p=False)
-        except AssertionError:
-            caught += 1
-    assert caught > 0
-
-
-@pytest.mark.parametrize("mutation", ["lag2_wait", "rescale_wait"])
-def test_bk128_d128_commit_waits_are_needed(mutation):
-    """d = 128 with P V commits arriving late: dropping the wait for P V(g-2) lets a
-    pv_done barrier run two phases ahead of a later wait, and dropping the wait
-    before a rescale lets O be rescaled while a product still adds to it: caught."""
+@pytest.mark.parametrize("mutation", [{"s_waits_free": False}, {"p_waits_pv": False},
+                                      {"one_exchange_buffer": True}])
+def test_bk128_mutations_are_caught(mutation):
+    """An S issuer that does not wait for the S buffer to be copied out, a softmax that
+    stores P (or rescales O) without waiting for the previous P V product, and a single
+    exchange buffer shared by consecutive exchanges: each caught."""
     from pipeline_model import simulate_bk128
 
     caught = 0
     for seed in range(30):
         try:
-            simulate_bk128(2048, False, _items128(2048, True), 3, 2, seed, True,
-                           rescale_prob=0.0 if mutation == "lag2_wait" else 0.3, late_weight=0.05,
-                           **{mutation: False})
+            simulate_bk128(2048, False, _items128(2048, True), 3, 2, seed, rescale_prob=0.3, late_weight=0.2,
+                           **mutation)
         except AssertionError:
             caught += 1
     assert caught > 0
