@@ -26,22 +26,24 @@
 // issued the P V product, which put about 1200 cycles of issue into every
 // block's dependency chain.)
 //
-// Softmax: both warpgroups work on one S at a time, in the issuing order.
-// Warpgroup h takes keys [64 h, 64 h + 64) of the block; thread r of each owns
-// query row r (TMEM lane r). The two halves of a row agree on the row maximum
-// through shared memory (warps q and q + 4 own the same 32 lanes and meet at an
-// mbarrier), so both keep the same reference maximum; each keeps its own
-// partial denominator, and the two are added at the epilogue.
+// Softmax: warpgroup t works on tile t; thread r owns query row r (TMEM lane r)
+// and all 128 keys of a block, so no two threads share a row. The two tiles'
+// S products alternate in the S buffer, so the two warpgroups' softmax passes
+// overlap in time: while one runs its exponent loop, the other loads, reduces
+// or stores. (Both warpgroups on one tile at a time, 64 keys each with the row
+// maximum exchanged through shared memory, ran the passes back to back: about
+// 1650 cycles per tile and block, nearly twice the tensor time.)
 //
 // Roles (16 warps, one persistent CTA per SM):
-//   warps 0-7   softmax + epilogue: warpgroup h = warp / 4 takes key half h
+//   warps 0-3   softmax + epilogue of query tile 0
+//   warps 4-7   softmax + epilogue of query tile 1
 //   warp  8     TMA producer: Q tiles per item, then K and V rings
 //   warp  9     S issuer: S_t(j) = Q_t K_j^T for t = 0, 1 in turn, into the S buffer
 //   warps 10-11 P V issuer of tile t = warp - 10: O_t += P_t(j) V_j
 //   warp  12    packed batch only: publishes the CTA's work items (ItemRing)
 //   warps 13-15 idle (they complete the last warpgroup)
-// Shared memory holds no static variables: the abort word, the item ring and
-// the row-maximum exchange live after the barriers in the dynamic region.
+// Shared memory holds no static variables: the abort word and the item ring
+// live after the barriers in the dynamic region.
 #pragma once
 #include "fa_fwd_kernel.cuh"
 
@@ -83,9 +85,7 @@ struct Cfg128 {
     // pv_done[2][2] drain
     static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 9 + 1;
     static constexpr int SMEM_TMEM_SLOT = SMEM_BAR + ((NUM_BARS * 8 + 15) / 16) * 16;
-    static constexpr int SMEM_XBAR = SMEM_TMEM_SLOT + 16;         // 4 exchange barriers (one per lane quadrant)
-    static constexpr int SMEM_XCH = SMEM_XBAR + 32;               // float [2 parity][2 halves][128 rows]
-    static constexpr int SMEM_RING = SMEM_XCH + 2 * 2 * 128 * 4;  // ItemRing (packed batches)
+    static constexpr int SMEM_RING = SMEM_TMEM_SLOT + 16;         // ItemRing (packed batches)
     static constexpr int SMEM_ABORT = SMEM_RING + 128;
     static constexpr int SMEM_USED = SMEM_ABORT + 16;
     // up to 1024 bytes to align the base (SW128 tiles need 1024-byte alignment), within the 227 KB limit
@@ -108,8 +108,8 @@ struct Sync128 {
     __device__ __forceinline__ uint32_t k_empty(int s) const { return at(4 + RK + s); }
     __device__ __forceinline__ uint32_t v_full(int s) const { return at(4 + 2 * RK + s); }
     __device__ __forceinline__ uint32_t v_empty(int s) const { return at(4 + 2 * RK + RV + s); }
-    // S ready for tile t (MMA commit), the S buffer copied out (256 softmax threads),
-    // P ready for tile t (256 softmax threads), P V_t(g) done (MMA commit to
+    // S ready for tile t (MMA commit), the S buffer copied out (the 128 threads of the
+    // tile's warpgroup), P ready for tile t (the same 128), P V_t(g) done (MMA commit to
     // pv_done(t, g & 1)). No barrier can get two phases ahead of a waiter (see the
     // roles below), so parity waits are exact.
     __device__ __forceinline__ uint32_t s_full(int t) const { return at(B0 + t); }
@@ -118,6 +118,21 @@ struct Sync128 {
     __device__ __forceinline__ uint32_t pv_done(int t, int b) const { return at(B0 + 5 + 2 * t + b); }
     __device__ __forceinline__ uint32_t drain() const { return at(B0 + 9); }
 };
+
+// Row maximum of 128 values: eight independent three-input chains, then a short tree.
+__device__ __forceinline__ float row_max128(const float (&x)[128]) {
+    float m8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+#pragma unroll
+    for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[120 + i]);
+    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
 
 template <typename T, int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -134,8 +149,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + pad;
     Sync128<RK, RV> sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_TMEM_SLOT);
-    float *xch = reinterpret_cast<float *>(smem + C::SMEM_XCH);
-    uint64_t *xbar = reinterpret_cast<uint64_t *>(smem + C::SMEM_XBAR);
     ItemRing *ring = reinterpret_cast<ItemRing *>(smem + C::SMEM_RING);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::SMEM_ABORT);
 
@@ -147,11 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.q_full(t), 1);
             mbar_init(sy.q_empty(t), 1);
             mbar_init(sy.s_full(t), 1);
-            mbar_init(sy.p_full(t), 2 * kBQ);  // both softmax warpgroups
+            mbar_init(sy.p_full(t), kBQ);  // the tile's softmax warpgroup
             mbar_init(sy.pv_done(t, 0), 1);
             mbar_init(sy.pv_done(t, 1), 1);
         }
-        mbar_init(sy.s_free(), 2 * kBQ);
+        mbar_init(sy.s_free(), kBQ);  // the warpgroup of the tile whose S the buffer holds
         for (int s = 0; s < RK; ++s) {  // a K slot is released by the S issuer
             mbar_init(sy.k_full(s), 1);
             mbar_init(sy.k_empty(s), 1);
@@ -161,7 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.v_empty(s), 2);
         }
         mbar_init(sy.drain(), 3);  // one commit per issuing warp
-        for (int q = 0; q < 4; ++q) mbar_init(smem_u32(xbar + q), 64);  // warps q and q + 4
         if constexpr (VARLEN) {
             for (int i = 0; i < kItemRing; ++i) {
                 mbar_init(smem_u32(&ring->full[i]), 1);
@@ -379,179 +391,138 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         setmaxnreg_inc<192>();
         // -------------------------------------------------------------- softmax + epilogue
-        constexpr int HK = kBK128 / 2;  // keys per half
-        constexpr int HD = D / 2;       // O columns per half
-        const int h = warp >> 2;        // key half of this warpgroup
-        const int qd = warp & 3;        // TMEM lane quadrant (warps qd and qd + 4 share it)
+        const int t = warp >> 2;  // query tile of this warpgroup
         const int r = threadIdx.x & 127;
-        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + C::TM_S;
+        const uint32_t p_addr = tmem + lane_base + C::TM_P + 64 * t;
+        const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t;
         const float scale_log2 = p.scale_log2;
         // raw scores scaled inside the exponent when the scale is positive (the maximum
         // commutes with it); otherwise pre-scaled scores (a -inf raw score times a
         // non-positive scale is not -inf)
         const bool fast = scale_log2 > 0.0f;
         const float sl2 = fast ? scale_log2 : 1.0f;
-        uint32_t xcount = 0;  // exchanges with the partner thread (phase of the pair's barrier)
-        // The partner (same row, other key half) receives v; returns the partner's value. The
-        // pair meets at an mbarrier with the same bounded wait as every pipeline wait (a warp
-        // that gives up does not leave its partner waiting forever). Buffers alternate by
-        // phase: a value is overwritten two exchanges later, after the partner has read it.
-        const uint32_t pair_bar = smem_u32(xbar + qd);
-        auto exchange = [&](float v, bool &okx) -> float {
-            float *buf = xch + (xcount & 1u) * 256;
-            buf[h * 128 + r] = v;
-            tc_fence_before();  // this thread's tensor-memory reads come before the partner's writes
-            mbar_arrive(pair_bar);
-            okx = wait_warp(pair_bar, xcount & 1u, abort_flag, p);
-            ++xcount;
-            tc_fence_after();
-            return buf[(h ^ 1) * 128 + r];
-        };
-        uint32_t scount[2] = {0, 0};  // S blocks consumed per tile (all items)
-        uint32_t g[2] = {0, 0};       // P blocks produced per tile = its P V products
+        uint32_t scount = 0;  // S products of this tile consumed (all items)
+        uint32_t g = 0;       // P blocks produced (all items) = P V products of this tile
         bool ok = true;
         ItemIter<VARLEN> iter(p, abort_flag, ring);
         for (Item itm; ok && iter.next(p, itm, ok);) {
             const int bh = itm.bh, q0 = itm.q0, n = itm.n;
-            const int nt[2] = {tile_nkv<CAUSAL, kBK128>(itm, 0), tile_nkv<CAUSAL, kBK128>(itm, 1)};
-            const int nmax = max(nt[0], nt[1]);
-            float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
-            for (int j = 0; ok && j < nmax; ++j) {
+            const int nt = tile_nkv<CAUSAL, kBK128>(itm, t);
+            if (nt == 0) continue;
+            const int row = q0 + t * kBQ + r;  // query row within the sequence (may be >= n in a ragged tail)
+            const int tile_row0 = q0 + t * kBQ;
+            float m_ref = -INFINITY, l = 0.0f;
+            for (int j = 0; j < nt; ++j, ++g) {
+                ok = wait_warp(sy.s_full(t), scount & 1u, abort_flag, p);
+                ++scount;
+                if (!ok) break;
+                tc_fence_after();
+                float x[128];
+                {
+                    uint32_t sr[128];
+                    tmem_ld128_wait(s_addr, sr);
+                    if (fast) {  // warp-uniform
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok || j >= nt[t]) continue;
-                    const uint32_t s_addr = tmem + lane_base + C::TM_S + HK * h;  // fp32 S columns of this half
-                    const uint32_t p_addr = tmem + lane_base + C::TM_P + 64 * t + HK / 2 * h;
-                    const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t + HD * h;
-                    ok = wait_warp(sy.s_full(t), scount[t] & 1u, abort_flag, p);
-                    ++scount[t];
-                    if (!ok) break;
-                    tc_fence_after();
-                    float x[HK];
-                    {
-                        uint32_t sr[HK];
-                        tmem_ld64_nowait(s_addr, sr);
-                        tmem_wait_ld_dep64(sr);
-                        if (fast) {  // warp-uniform
+                        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+                    } else {
 #pragma unroll
-                            for (int c = 0; c < HK; ++c) x[c] = __uint_as_float(sr[c]);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < HK; ++c) x[c] = __uint_as_float(sr[c]) * scale_log2;
-                        }
+                        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]) * scale_log2;
                     }
-                    tc_fence_before();
-                    mbar_arrive(sy.s_free());  // the S buffer may now take the next product
-                    // keys past the end of the sequence, and (causal) keys after the query
-                    const int row = q0 + t * kBQ + r;  // query row within the sequence (may be >= n)
-                    const int kbase = j * kBK128 + HK * h;
-                    const bool ragged = kbase + HK > n;
-                    const bool diag = CAUSAL && (kbase + HK - 1 > q0 + t * kBQ);
-                    if (ragged || diag) {
-                        int lim = n - 1 - kbase;
-                        if (CAUSAL) lim = min(lim, row - kbase);
+                }
+                tc_fence_before();
+                mbar_arrive(sy.s_free());  // the S buffer may now take the next product
+                // keys past the end of the sequence, and (causal) keys after the query
+                const int kbase = j * kBK128;
+                const bool ragged = kbase + kBK128 > n;
+                const bool diag = CAUSAL && (kbase + kBK128 - 1 > tile_row0);
+                if (ragged || diag) {
+                    int lim = n - 1 - kbase;
+                    if (CAUSAL) lim = min(lim, row - kbase);
 #pragma unroll
-                        for (int c = 0; c < HK; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
-                    }
-                    float m8[8];
+                    for (int c = 0; c < 128; ++c) x[c] = (c > lim) ? -INFINITY : x[c];
+                }
+                const float mb = row_max128(x) * sl2;  // sl2 > 0
+                const float m_new = fmaxf(m_ref, mb);
+                // lazy rescale: move the reference only when the maximum grew by more than TAU
+                const bool need = (m_new > m_ref + kTau) || (m_ref == -INFINITY && m_new != -INFINITY);
+                const float alpha = need ? ex2_approx(m_ref - m_new) : 1.0f;  // 2^-inf = 0
+                const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
+                if (need) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                const float neg = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+                const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
+                float2 ls[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                make_float2(0.0f, 0.0f)};
+                // P in two halves of 64 keys (32 packed columns each), each stored as soon as it is ready
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(x[i], x[8 + i], x[16 + i]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pv[32];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[24 + i], x[32 + i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[40 + i], x[48 + i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[56 + i]);
-                    const float mhalf =
-                        fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                    const float mother = exchange(mhalf, ok);
-                    if (!ok) break;
-                    const float mb = fmaxf(mhalf, mother) * sl2;  // sl2 > 0
-                    const float m_new = fmaxf(m_ref[t], mb);
-                    // lazy rescale: move the reference only when the maximum grew by more than TAU
-                    const bool need = (m_new > m_ref[t] + kTau) || (m_ref[t] == -INFINITY && m_new != -INFINITY);
-                    const float alpha = need ? ex2_approx(m_ref[t] - m_new) : 1.0f;  // 2^-inf = 0
-                    const bool rescale = __any_sync(0xffffffffu, need) && j > 0;
-                    if (need) {
-                        l[t] *= alpha;
-                        m_ref[t] = m_new;
-                    }
-                    const float neg = (m_ref[t] == -INFINITY) ? 0.0f : -m_ref[t];
-                    const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
-                    float2 ls[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                                    make_float2(0.0f, 0.0f)};
-                    uint32_t pv[HK / 2];
-#pragma unroll
-                    for (int c = 0; c < HK / 2; ++c) {
-                        const float2 a = ffma2(make_float2(x[2 * c], x[2 * c + 1]), sl2v, negv);
+                    for (int c = 0; c < 32; ++c) {
+                        const int i = 64 * hh + 2 * c;
+                        const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
                         const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                         ls[c & 3] = fadd2(ls[c & 3], e);
                         pv[c] = pack2<T>(e.x, e.y);
                     }
-                    l[t] += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
-                    // P V(g-1), the tile's previous product, read P_t and accumulated into O_t: wait
-                    // for its commit before overwriting P_t and before rescaling O_t. (It was issued
-                    // when P_t(g-1) was released, a whole block of both tiles ago.)
-                    if (g[t] > 0) {
-                        ok = wait_warp(sy.pv_done(t, (g[t] - 1) & 1u), ((g[t] - 1) >> 1) & 1u, abort_flag, p);
+                    // P V(g-1), the tile's previous product, read P_t and accumulated into O_t:
+                    // wait for its commit before overwriting P_t (and before rescaling O_t below).
+                    if (hh == 0 && g > 0) {
+                        ok = wait_warp(sy.pv_done(t, (g - 1) & 1u), ((g - 1) >> 1) & 1u, abort_flag, p);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    tmem_st32(p_addr, pv);
-                    if (rescale) {
-                        // O holds P V for blocks < j relative to the old reference: scale this half's
-                        // columns of the row (alpha = 1 where the reference did not move)
-#pragma unroll
-                        for (int c0 = 0; c0 < HD; c0 += 32) {
-                            uint32_t ov[32];
-                            tmem_ld32_wait(o_addr + c0, ov);
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-                            tmem_st32(o_addr + c0, ov);
-                        }
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(sy.p_full(t));
-                    ++g[t];
+                    tmem_st32(p_addr + 32 * hh, pv);
                 }
+                if (!ok) break;
+                l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+                if (rescale) {
+                    // O holds P V for blocks < j relative to the old reference: scale its rows
+                    // (alpha = 1 for rows whose reference did not move) before P V(j) adds to it
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32_wait(o_addr + c0, ov);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+                        tmem_st32(o_addr + c0, ov);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(sy.p_full(t));
             }
             if (!ok) break;
-            // ---------------------------------------------------------- epilogue, tile by tile
+            // ---------------------------------------------------------- epilogue
+            ok = wait_warp(sy.pv_done(t, (g - 1) & 1u), ((g - 1) >> 1) & 1u, abort_flag, p);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+            const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
+                                           : ((size_t)bh * p.N + (size_t)row);
+            T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (!ok || nt[t] == 0) continue;
-                const float l_other = exchange(l[t], ok);  // the other half's partial denominator
-                if (!ok) break;
-                const float l_row = l[t] + l_other;
-                ok = wait_warp(sy.pv_done(t, (g[t] - 1) & 1u), ((g[t] - 1) >> 1) & 1u, abort_flag, p);
-                if (!ok) break;
-                tc_fence_after();
-                const int row = q0 + t * kBQ + r;
-                const uint32_t o_addr = tmem + lane_base + C::TM_O + D * t + HD * h;
-                const float inv = (l_row > 0.0f) ? 1.0f / l_row : 0.0f;
-                const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
-                                               : ((size_t)bh * p.N + (size_t)row);
-                T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D + HD * h;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32_wait(o_addr + c0, ov);
+                if (row < n) {
 #pragma unroll
-                for (int c0 = 0; c0 < HD; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32_wait(o_addr + c0, ov);
-                    if (row < n) {
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8)
-                            st_global_v4(orow + c0 + c,
-                                         pack2<T>(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv),
-                                         pack2<T>(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv),
-                                         pack2<T>(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv),
-                                         pack2<T>(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv));
-                    }
+                    for (int c = 0; c < 32; c += 8)
+                        st_global_v4(orow + c0 + c,
+                                     pack2<T>(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv),
+                                     pack2<T>(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv),
+                                     pack2<T>(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv),
+                                     pack2<T>(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv));
                 }
-                tc_fence_before();  // the O reads come before the next item's first P V (after p_full)
-                if (h == 0 && row < n)
-                    p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
-                        (l_row > 0.0f) ? (m_ref[t] + lg2_approx(l_row)) * 0.6931471805599453f : -INFINITY;
             }
+            tc_fence_before();  // the O reads above come before the next item's first P V (after p_full)
+            if (row < n)  // lse: [B][H][N], or [H][total] for a packed batch
+                p.lse[VARLEN ? (size_t)(bh % p.H) * p.total + itm.tok0 + row : (size_t)bh * p.N + row] =
+                    (l > 0.0f) ? (m_ref + lg2_approx(l)) * 0.6931471805599453f : -INFINITY;
         }
     }
 

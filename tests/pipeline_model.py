@@ -415,16 +415,15 @@ def simulate_bwd_halves(n_it, stages, seed):
 
 
 def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0, s_waits_free=True,
-                   p_waits_pv=True, late_weight=1.0, one_exchange_buffer=False):
+                   p_waits_pv=True, late_weight=1.0):
     """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
     the S issuer (S_t(j) for t = 0, 1 in turn into the one S buffer), one P V
     issuer per tile, the eight softmax warps and (``item_ring`` > 0) the
     packed-batch item list.
 
-    The softmax warps take the S products in issue order: warp w = 4 h + q takes
-    key half h of TMEM lane quadrant q; warps q and q + 4 (the same rows) exchange
-    their row maxima at the pair barrier x{q} before computing P (buffers by
-    exchange parity), and their partial denominators at the epilogue.
+    Softmax warp w = 4 t + q handles the rows of TMEM lane quadrant q of tile t,
+    all 128 keys of each block; the four warps of tile t copy out each of the
+    tile's S products and release the S buffer.
 
     Besides the barrier checks of ``simulate`` the model tracks the S buffer and
     each tile's P buffer, so that an S product that overwrites an S the softmax
@@ -437,9 +436,7 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
 
     Mutations that must be caught: ``s_waits_free=False`` (the S issuer does not
     wait for the S buffer to be copied out), ``p_waits_pv=False`` (the softmax
-    stores P_t(g) without waiting for P V_t(g-1), and rescales O without it),
-    ``one_exchange_buffer=True`` (one exchange buffer instead of one per parity:
-    a fast pair member overwrites a value its partner has not read)."""
+    stores P_t(g) without waiting for P V_t(g-1), and rescales O without it)."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
@@ -449,18 +446,16 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
         B[name] = Bar(name, count)
 
     for t in range(2):
-        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("p_full", 2 * BQ), ("pv_done0", 1),
+        for name, c in (("q_full", 1), ("q_empty", 1), ("s_full", 1), ("p_full", BQ), ("pv_done0", 1),
                         ("pv_done1", 1)):
             bar(f"{name}{t}", c)
-    bar("s_free", 2 * BQ)
+    bar("s_free", BQ)
     for s_ in range(rk):
         bar(f"k_full{s_}", 1)
         bar(f"k_empty{s_}", 1)
     for s_ in range(rv):
         bar(f"v_full{s_}", 1)
         bar(f"v_empty{s_}", 2)
-    for q in range(4):
-        bar(f"x{q}", 64)
     consumers = 4 + NW
     for s_ in range(item_ring):
         bar(f"item_full{s_}", 1)
@@ -471,9 +466,8 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
     o_last = [None, None]    # per tile: the last P V product executed
     sbuf = [None]            # the S buffer: (tile, block index of the tile)
     sreads = {}              # (tile, g) -> softmax warps that copied it out
-    pbuf = [[[None] * 2 for _ in range(4)] for _ in range(2)]  # per tile, quadrant, half: ("P", g)
+    pbuf = [[None] * 4 for _ in range(2)]  # per tile and lane quadrant: ("P", g)
     pv_read = [set(), set()]
-    xbuf = [[[(-1, None)] * 2 for _ in range(2)] for _ in range(4)]  # [quadrant][parity][half]
 
     def nkv(n_seq, q0, t):
         r0 = q0 + t * BQ
@@ -571,62 +565,43 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
         yield from take(len(items))
 
     def softmax(w):
-        h, q = w // 4, w % 4
-        scount, g = [0, 0], [0, 0]
-        xk = [0]
-
-        def exchange():
-            k = xk[0]
-            par = 0 if one_exchange_buffer else k & 1
-            xbuf[q][par][h] = (k, w)
-            yield ("arrive", f"x{q}", 32)
-            yield ("wait", f"x{q}", k)
-            other = xbuf[q][par][1 - h]
-            assert other[0] == k, f"quadrant {q}: exchange {k} reads {other} from the other half"
-            xk[0] += 1
-
+        t, q = w // 4, w % 4
+        scount = g = 0
         for i, q0 in enumerate(items):
             yield from take(i)
-            n, nmax = counts(q0)
-            for j in range(nmax):
-                for t in range(2):
-                    if j >= n[t]:
-                        continue
-                    yield ("wait", f"s_full{t}", scount[t])
-                    scount[t] += 1
-                    assert sbuf[0] == (t, g[t]), f"softmax {w} expects S({t}, {g[t]}) but the buffer holds {sbuf[0]}"
-                    sreads[(t, g[t])] = sreads.get((t, g[t]), 0) + 1
-                    yield ("arrive", "s_free", 32)
-                    yield from exchange()
-                    if g[t] > 0 and p_waits_pv:
-                        yield ("wait", f"pv_done{t}{(g[t] - 1) & 1}", (g[t] - 1) >> 1)
-                    cell = pbuf[t][q][h]
-                    assert cell is None or cell[1] in pv_read[t], (
-                        f"tile {t}: P({g[t]}) overwrites P{cell} before its P V product read it")
-                    pbuf[t][q][h] = ("P", g[t])
-                    if j > 0 and rnd.random() < rescale_prob:
-                        assert o_done[t] >= g[t] - 1, f"tile {t}: O rescaled before P V({g[t] - 1}) is done"
-                    yield ("arrive", f"p_full{t}", 32)
-                    g[t] += 1
-            for t in range(2):
-                if not n[t]:
-                    continue
-                yield from exchange()
-                yield ("wait", f"pv_done{t}{(g[t] - 1) & 1}", (g[t] - 1) >> 1)  # epilogue
-                assert o_done[t] == g[t] - 1, f"tile {t}: the epilogue reads O with P V done up to {o_done[t]}"
-                assert o_last[t] == g[t] - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]})"
+            n, _ = counts(q0)
+            if not n[t]:
+                continue
+            for j in range(n[t]):
+                yield ("wait", f"s_full{t}", scount)
+                scount += 1
+                assert sbuf[0] == (t, g), f"softmax {w} expects S({t}, {g}) but the buffer holds {sbuf[0]}"
+                sreads[(t, g)] = sreads.get((t, g), 0) + 1
+                yield ("arrive", "s_free", 32)
+                if g > 0 and p_waits_pv:
+                    yield ("wait", f"pv_done{t}{(g - 1) & 1}", (g - 1) >> 1)
+                cell = pbuf[t][q]
+                assert cell is None or cell[1] in pv_read[t], (
+                    f"tile {t}: P({g}) overwrites P{cell} before its P V product read it")
+                pbuf[t][q] = ("P", g)
+                if j > 0 and rnd.random() < rescale_prob:
+                    assert o_done[t] >= g - 1, f"tile {t}: O rescaled before P V({g - 1}) is done"
+                yield ("arrive", f"p_full{t}", 32)
+                g += 1
+            yield ("wait", f"pv_done{t}{(g - 1) & 1}", (g - 1) >> 1)  # epilogue
+            assert o_done[t] == g - 1, f"tile {t}: the epilogue reads O with P V done up to {o_done[t]}"
+            assert o_last[t] == g - 1, f"tile {t}: the epilogue reads O after P V({o_last[t]})"
         yield from take(len(items))
 
     def execute(kind, t, g):
         if kind == "S":
             prev = sbuf[0]
-            assert prev is None or sreads.get(prev, 0) == NW, (
-                f"S({t}, {g}) overwrites S{prev} copied out by {sreads.get(prev, 0)} of {NW} warps")
+            assert prev is None or sreads.get(prev, 0) == 4, (
+                f"S({t}, {g}) overwrites S{prev} copied out by {sreads.get(prev, 0)} of 4 warps")
             sbuf[0] = (t, g)
         else:
-            for q in range(4):
-                for cell in pbuf[t][q]:
-                    assert cell == ("P", g), f"tile {t}: P V({g}) reads {cell}"
+            for cell in pbuf[t]:
+                assert cell == ("P", g), f"tile {t}: P V({g}) reads {cell}"
             pv_read[t].add(g)
             o_last[t] = g
 
