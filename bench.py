@@ -46,7 +46,8 @@ from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, GQA
 
 METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (B=1,H=32,N=8192,d=128 causal)"
 UNIT = "TFLOP/s"
-KERNEL_SOURCES = ["io_aware_exact_13_gb300/csrc/fa_fwd_kernel.cuh", "io_aware_exact_13_gb300/csrc/ptx.cuh",
+KERNEL_SOURCES = ["io_aware_exact_13_gb300/csrc/fa_fwd_bk128.cuh", "io_aware_exact_13_gb300/csrc/fa_fwd_kernel.cuh",
+                  "io_aware_exact_13_gb300/csrc/ptx.cuh",
                   "io_aware_exact_13_gb300/csrc/fa_launch.cuh"]
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -101,10 +102,10 @@ def load_peak():
         return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16 (no measured peak file)"
 
 
-def load_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload, if
-    it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_kernel_{workload}.md")
+def load_traffic(workload: str, kernel: str = "fa_fwd_bk128_kernel"):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         txt = open(path).read()
     except OSError:
@@ -373,9 +374,16 @@ def run_ours(args, w):
     peak, peak_src = load_peak()
     mean_launch_s = statistics.mean(launch_ms) * 1e-3
     achieved = w.flops / mean_launch_s / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(w.name), "peak_source": peak_src,
-                "kernel": "fa_fwd_kernel", "launch_ms_mean": 1e3 * mean_launch_s,
+    if w.dtype == "fp32":
+        # CUDA-core FFMA path: 128 fp32 FMA lanes per SM (2 flop each) at the maximum SM clock
+        peak, peak_src = 2 * 128 * fa.fa_num_sms() * 2.07e9 / 1e12, "fp32 FFMA rate at 2070 MHz (unit counts)"
+    roofline = {"bound": "alu" if w.dtype == "fp32" else "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(w.name, "fa_fwd_kernel" if w.has_mask else "fa_fwd_bk128_kernel"),
+                "peak_source": peak_src,
+                "kernel": ("fa_fwd_kernel (64-key blocks, additive mask)" if w.has_mask
+                           else "fa_fwd_fp32_kernel" if w.dtype == "fp32" else "fa_fwd_bk128_kernel"),
+                "launch_ms_mean": 1e3 * mean_launch_s,
                 "launch_ms_median": statistics.median(launch_ms),
                 "launch_ms_min": min(launch_ms), "launch_ms_max": max(launch_ms)}
     # second denominator: the tensor core's own rate (8192 flop/clk/SM for dense 16-bit MMAs, measured at
