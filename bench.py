@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
+from io_aware_exact_13_gb300.shard import head_range  # noqa: E402
 from io_aware_exact_13_gb300.inputs import (BWD_WORKLOADS, DECODE_WORKLOADS, GQA_WORKLOADS, HEADLINE,  # noqa: E402
                                             VARLEN_WORKLOADS, WORKLOADS, make_bwd, make_decode, make_gqa,
                                             make_varlen, make_workload, sample_rows)
@@ -69,12 +70,14 @@ def needs_flush(w) -> bool:
     return workload_bytes(w) < 2 * L2_BYTES
 
 
-def bench_config(w, world: int) -> dict:
+def bench_config(w, world: int, split: bool = False) -> dict:
     """The ``config`` object of both arms' JSON lines (the same workload, the same keys)."""
     mb = workload_bytes(w) / 1e6
     l2 = (f"inputs and outputs ({mb:.0f} MB) exceed the 126 MB L2; no flush between steps" if not needs_flush(w)
           else f"inputs and outputs ({mb:.1f} MB) fit in L2; a 256 MB buffer is written between timed steps")
-    return dict(w.describe(), l2=l2, parallelism=f"replicas x{world} (independent problems, no collective)")
+    par = (f"heads split over {world} ranks (one problem, no collective)" if split
+           else f"replicas x{world} (independent problems, no collective)")
+    return dict(w.describe(), l2=l2, parallelism=par)
 
 
 def kernel_source_hash() -> str:
@@ -270,10 +273,17 @@ def run_ours(args, w):
 
     entry = {"bf16": fa.fa_fwd, "fp16": fa.fa_fwd_fp16, "fp32": fa.fa_fwd_fp32}[w.dtype]
     q, k, v, mask = make_workload(w)
+    # --partition heads: this rank computes heads [h0, h1) of every batch index of the one problem
+    # (strong scaling, no collective); otherwise every rank computes the whole problem (replicas)
+    split = args.partition == "heads" and world > 1
+    h0, h1 = head_range(w.H, world, rank) if split else (0, w.H)
+    if split:
+        q, k, v = (t[:, h0:h1].contiguous() for t in (q, k, v))
+    units_rank = w.flops * (h1 - h0) / w.H
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     md = None if mask is None else mask.to(dev)
     od = torch.empty_like(qd)
-    lsed = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    lsed = torch.empty((w.B, h1 - h0, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -328,7 +338,9 @@ def run_ours(args, w):
     if status != 0:
         raise SystemExit(f"device status word {status} after the timed region")
     ms_per_step = total_ms / args.steps
-    value = whole_job_rate(world, w.flops * args.steps, total_ms) / 1e12
+    # the whole job: every rank's units (a replica each, or a share of one problem) over the slowest rank's time
+    job_units = (w.flops if split else world * w.flops) * args.steps
+    value = job_units / (total_ms * 1e-3) / 1e12
 
     # ---------------------------------------------------------------- end to end through host buffers
     qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
@@ -366,6 +378,7 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     barrier(world, dev)
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1), dev) / e2e_steps
+    job_flops = w.flops if split else world * w.flops
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh) + ((mh,) if mh is not None else ()))
     d2h = oh.numel() * oh.element_size() + lh.numel() * 4
 
@@ -373,7 +386,7 @@ def run_ours(args, w):
         return 0
     peak, peak_src = load_peak()
     mean_launch_s = statistics.mean(launch_ms) * 1e-3
-    achieved = w.flops / mean_launch_s / 1e12
+    achieved = units_rank / mean_launch_s / 1e12
     if w.dtype == "fp32":
         # CUDA-core FFMA path: 128 fp32 FMA lanes per SM (2 flop each) at the maximum SM clock
         peak, peak_src = 2 * 128 * fa.fa_num_sms() * 2.07e9 / 1e12, "fp32 FFMA rate at 2070 MHz (unit counts)"
@@ -395,15 +408,15 @@ def run_ours(args, w):
         roofline["frac_at_sampled_clock"] = achieved / at_clock
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic",
-        "config": bench_config(w, world),
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "strong" if split else "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": bench_config(w, world, split),
         "timing": {"repeats": len(rep_ms), "ms_per_step_median": ms_per_step,
                    "ms_per_step_min": min(rep_ms) / args.steps, "ms_per_step_max": max(rep_ms) / args.steps,
                    "timed_s": sum(rep_ms) * 1e-3,
                    "ms_x_mhz": (ms_per_step * clocks["sm_mhz"]) if clocks and clocks.get("sm_mhz") else None},
         "pct_of_peak": 100.0 * value / (world * peak),
-        "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": (f"fa_fwd_host, {E2E_CHUNKS} head chunks, copies pipelined with the forward"
                          if host_entry is not None else "copy in, fa_fwd, copy out")},
@@ -720,6 +733,9 @@ def main():
     ap.add_argument("--timed-s", type=float, default=2.0,
                     help="repeat the K-step timed region until about this many seconds are covered")
     ap.add_argument("--max-repeats", type=int, default=200)
+    ap.add_argument("--partition", choices=["replicas", "heads"], default="replicas",
+                    help="N>1: every rank runs the whole workload (replicas, weak scaling) or one share of its "
+                         "heads (heads, strong scaling)")
     ap.add_argument("--no-materialised", action="store_true",
                     help="backward workloads: skip the materialised comparison leg")
     args = ap.parse_args()
