@@ -103,6 +103,20 @@ int fa_fwd_gqa(const void *q, const void *k, const void *v, const float *mask_or
 int fa_fwd_gqa_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out,
                     float *lse, int B, int H, int Hkv, int N, int d, float scale, int causal, void *stream);
 
+/* ---- per-head additive bias -------------------------------------------------
+ * Same operation as fa_fwd / fa_fwd_fp16 with the additive term M given per head:
+ * bias is float [B][H][N][N] (DEVICE, 16-byte aligned, required), and score
+ * (b, h, i, j) = scale q_i k_j^T + bias[b][h][i][j] (+ the causal term). Entries
+ * are finite or -inf; a row whose every key is -inf gets out = 0 and lse = -inf.
+ * ("IO-aware exact attention", section "Why implementations form a family":
+ * bias is one of the variants that modify the calculation; "FlashAttention"
+ * glossary, section "Move less data", for the additive M.) Errors as for fa_fwd;
+ * FA_ERR_NULL if bias is NULL. */
+int fa_fwd_bias(const void *q, const void *k, const void *v, const float *bias, void *out, float *lse, int B, int H,
+                int N, int d, float scale, int causal, void *stream);
+int fa_fwd_bias_fp16(const void *q, const void *k, const void *v, const float *bias, void *out, float *lse, int B,
+                     int H, int N, int d, float scale, int causal, void *stream);
+
 /* ---- split-KV forward for decoding ------------------------------------------
  * Same operation for Nq query rows (1 <= Nq <= 16) against Nk >= 1 keys:
  *   q, out : [B][H][Nq][d]      k, v : [B][H][Nk][d]      lse : float [B][H][Nq]

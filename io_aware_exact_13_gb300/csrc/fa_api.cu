@@ -120,14 +120,16 @@ int check_args(Type ty, const void *q, const void *k, const void *v, const float
 }
 
 int fwd_common(Type ty, const void *q, const void *k, const void *v, const float *mask, void *out, float *lse,
-               int B, int H, int N, int d, float scale, int causal, void *stream, int Hkv = -1) {
+               int B, int H, int N, int d, float scale, int causal, void *stream, int Hkv = -1,
+               int mask_per_head = 0) {
     int rc = check_args(ty, q, k, v, mask, out, lse, B, H, N, d);
     if (rc != FA_OK) return rc;
     if (Hkv == -1) Hkv = H;
     if (Hkv < 1 || H % Hkv != 0) return FA_ERR_SHAPE;
-    log_call("forward %s d=%d causal=%d mask=%d B=%d H=%d Hkv=%d N=%d scale=%g",
+    log_call("forward %s d=%d causal=%d mask=%s B=%d H=%d Hkv=%d N=%d scale=%g",
              ty == Type::BF16 ? "bf16 tcgen05" : ty == Type::FP16 ? "fp16 tcgen05" : "fp32 cuda-core", d,
-             causal ? 1 : 0, mask != nullptr, B, H, Hkv, N, static_cast<double>(scale));
+             causal ? 1 : 0, mask == nullptr ? "none" : mask_per_head ? "per-head bias" : "shared", B, H, Hkv, N,
+             static_cast<double>(scale));
     DeviceInfo *di = device_info();
     if (!di || !encoder()) return FA_ERR_LAUNCH;
     fa::LaunchArgs a;
@@ -148,6 +150,7 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
     a.status = di->status;
     a.num_sms = di->num_sms;
     a.timeout_ns = kDefaultTimeoutNs;
+    a.mask_per_head = mask_per_head;
     switch (ty) {
         case Type::BF16: rc = fa::launch_fwd_bf16(a); break;
         case Type::FP16: rc = fa::launch_fwd_fp16(a); break;
@@ -505,6 +508,18 @@ int fa_fwd_splitkv_fp16(const void *q, const void *k, const void *v, void *out, 
                         unsigned long long workspace_bytes, void *stream) {
     return splitkv_common(true, q, k, v, out, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace,
                           workspace_bytes, stream);
+}
+
+int fa_fwd_bias(const void *q, const void *k, const void *v, const float *bias, void *out, float *lse, int B, int H,
+                int N, int d, float scale, int causal, void *stream) {
+    if (!bias) return FA_ERR_NULL;
+    return fwd_common(Type::BF16, q, k, v, bias, out, lse, B, H, N, d, scale, causal, stream, -1, 1);
+}
+
+int fa_fwd_bias_fp16(const void *q, const void *k, const void *v, const float *bias, void *out, float *lse, int B,
+                     int H, int N, int d, float scale, int causal, void *stream) {
+    if (!bias) return FA_ERR_NULL;
+    return fwd_common(Type::FP16, q, k, v, bias, out, lse, B, H, N, d, scale, causal, stream, -1, 1);
 }
 
 int fa_fwd_gqa(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,

@@ -130,6 +130,7 @@ struct FwdParams {
     int total;              // tokens in the batch
     int Hkv;                // key/value heads
     int mask_tma;           // 1: the mask tensor map is valid (N % 4 == 0) and mask blocks arrive by TMA
+    int mask_per_head;      // 1: the mask is a per-head bias [B][H][N][N]; 0: [B][N][N] shared by the heads
 };
 
 // Static schedule: CTA c takes item w*G + c in even waves w and w*G + (G-1-c)
@@ -705,6 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nt == 0) continue;
             const int row = q0 + t * kBQ + r;  // global query row (may be >= N in a ragged tail)
             const int b = bh / p.H;
+            const int mz = p.mask_per_head ? bh : b;  // the mask's [B] or [B][H] slab of this item
             // HAS_MASK (mask_tma): the warp's 32 rows x 64 mask values of a key block arrive by two TMA
             // boxes (32 rows x 32 fp32, 128-byte swizzle; rows past N and keys past N read as 0) into the
             // warp's 8 KB staging area, issued while the block before it is processed
@@ -715,8 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint32_t bar = smem_u32(mask_bars() + warp);
                     mbar_arrive_expect_tx(bar, 2 * 32 * 128);
-                    tma_load_3d(mwarp, &tm_m, bar, jj * kBK, mrow0, b, mpol);
-                    tma_load_3d(mwarp + 4096, &tm_m, bar, jj * kBK + 32, mrow0, b, mpol);
+                    tma_load_3d(mwarp, &tm_m, bar, jj * kBK, mrow0, mz, mpol);
+                    tma_load_3d(mwarp + 4096, &tm_m, bar, jj * kBK + 32, mrow0, mz, mpol);
                 }
                 __syncwarp();
                 mpending = true;
@@ -739,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kbase = j * kBK;
                 if constexpr (HAS_MASK) {
                     const bool row_ok = row < p.N;
-                    const float *mrow = p.mask + ((size_t)b * p.N + (size_t)(row_ok ? row : 0)) * p.N + kbase;
+                    const float *mrow = p.mask + ((size_t)mz * p.N + (size_t)(row_ok ? row : 0)) * p.N + kbase;
                     if (p.mask_tma) {  // warp-uniform
                         ok = wait_warp(smem_u32(mask_bars() + warp), mcount & 1u, abort_flag, p);
                         if (!ok) break;

@@ -26,6 +26,7 @@ struct LaunchArgs {
     // packed variable-length batch (B = number of sequences, N = max_seqlen)
     const int *cu_seqlens = nullptr;
     int total = 0;
+    int mask_per_head = 0;  // the mask is a per-head bias [B][H][N][N]
 };
 
 // Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with box_rows-row x
@@ -71,7 +72,9 @@ int launch_variant(const LaunchArgs &a) {
     // multiple of 16 bytes (N % 4 == 0), otherwise the softmax warps read it directly
     CUtensorMap tm = tq;
     const bool mask_tma = MASK && a.mask && (a.N % 4) == 0;
-    if (mask_tma && !encode_rows_map(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.mask, a.N, a.N, a.B, 32)) return -5;
+    if (mask_tma && !encode_rows_map(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.mask, a.N, a.N,
+                                     a.mask_per_head ? BH : a.B, 32))
+        return -5;
     FwdParams p;
     p.out = a.out;
     p.lse = a.lse;
@@ -90,6 +93,7 @@ int launch_variant(const LaunchArgs &a) {
     p.total = 0;
     p.Hkv = a.Hkv;
     p.mask_tma = mask_tma ? 1 : 0;
+    p.mask_per_head = a.mask_per_head;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tm, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;

@@ -49,6 +49,8 @@ SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa_get_device_status": (ctypes.c_int, [_vp]),
     "fa_num_sms": (ctypes.c_int, []),
+    "fa_fwd_bias": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp]),
+    "fa_fwd_bias_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_gqa": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_gqa_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int] * 5),
@@ -206,6 +208,39 @@ def fa_fwd_gqa(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
 def fa_fwd_gqa_fp16(q, k, v, mask_or_null, out, lse, scale, causal, stream=None):
     """fp16 grouped-query forward."""
     _fwd_gqa("fa_fwd_gqa_fp16", torch.float16, q, k, v, mask_or_null, out, lse, scale, causal, stream)
+
+
+# ---------------------------------------------------------------- per-head additive bias
+def _fwd_bias(fn_name, dtype, q, k, v, bias, out, lse, scale, causal, stream):
+    B, H, N, d = _check(q, k, v, None, out, lse, dtype)
+    if (bias is None or bias.dtype != torch.float32 or bias.shape != (B, H, N, N) or not bias.is_contiguous()
+            or not bias.is_cuda):
+        raise ValueError("bias must be a contiguous CUDA float32 [B, H, N, N] tensor")
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse), B, H, N, d, float(scale),
+                               int(bool(causal)), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_bias(q, k, v, bias, out, lse, scale, causal, stream=None):
+    """bf16 forward with a per-head additive bias [B, H, N, N] (fp32)."""
+    _fwd_bias("fa_fwd_bias", torch.bfloat16, q, k, v, bias, out, lse, scale, causal, stream)
+
+
+def fa_fwd_bias_fp16(q, k, v, bias, out, lse, scale, causal, stream=None):
+    """fp16 forward with a per-head additive bias [B, H, N, N] (fp32)."""
+    _fwd_bias("fa_fwd_bias_fp16", torch.float16, q, k, v, bias, out, lse, scale, causal, stream)
+
+
+def attention_bias(q, k, v, bias, scale=None, causal=False, stream=None):
+    """Forward with a per-head additive bias; allocates O and lse."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fn = {torch.bfloat16: fa_fwd_bias, torch.float16: fa_fwd_bias_fp16}[q.dtype]
+    fn(q, k, v, bias, out, lse, scale, causal, stream)
+    return out, lse
 
 
 # ---------------------------------------------------------------- split-KV decoding

@@ -116,6 +116,26 @@ def attention(q, k, v, mask=None, scale=None, causal=False):
     return out, lse
 
 
+def attention_bias(q, k, v, bias, scale=None, causal=False):
+    """Attention with a per-head additive bias [B, H, Nq, Nk]: head h of every batch
+    index is the shared-mask definition above run on that head alone with mask
+    bias[:, h] ("IO-aware exact attention", section "Why implementations form a
+    family", names bias as a variant; the glossary's additive M, per head).
+    Returns (out [B,H,Nq,d], lse [B,H,Nq])."""
+    q, k, v, bias = _f64(q), _f64(k), _f64(v), _f64(bias)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if bias.shape != (B, H, Nq, Nk):
+        raise ValueError(f"bias must be [B, H, Nq, Nk] = {(B, H, Nq, Nk)}, got {bias.shape}")
+    out = np.zeros((B, H, Nq, d))
+    lse = np.zeros((B, H, Nq))
+    for h in range(H):
+        o, l = attention(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], mask=bias[:, h], scale=scale, causal=causal)
+        out[:, h] = o[:, 0]
+        lse[:, h] = l[:, 0]
+    return out, lse
+
+
 def attention_rows(q, k, v, rows, mask=None, scale=None, causal=False):
     """Materialised fp64 attention for flat row ids (b*H + h)*Nq + i.
     Returns (out [len(rows), d], lse [len(rows)])."""

@@ -173,6 +173,35 @@ def test_closed_form_additive_mask(oracle_lib):
     assert np.all(out[0, 0, 1] == 0.0) and lse[0, 0, 1] == -math.inf  # fully masked row
 
 
+def test_closed_form_per_head_bias(oracle_lib):
+    """Per-head bias [B, H, Nq, Nk]: every (b, h) gets its own integer bias matrix C
+    (0 = -inf), so its weights are w_j u_j^i C[b][h][i][j]; a bias applied to the wrong
+    head, batch index or row/key order breaks one of the closed forms."""
+    B, H, nq = 2, 3, 3
+    wk, uk = [1, 2, 3, 4], [2, 1, 1, 3]
+    rng = np.random.default_rng(11)
+    vals = [[[[int(x) for x in rng.integers(-5, 6, size=2)] for _ in range(4)] for _ in range(H)] for _ in range(B)]
+    C = rng.integers(0, 4, size=(B, H, nq, 4))
+    C[0, 1, 2] = 0  # one fully masked row
+    qd, kd = _design(wk, uk, nq)
+    q = np.broadcast_to(qd, (B, H, nq, 2)).copy()
+    k = np.broadcast_to(kd, (B, H, 4, 2)).copy()
+    v = np.array(vals, dtype=np.float64)
+    bias = np.where(C > 0, np.log(np.maximum(C, 1)), -math.inf)
+    out, lse = oracle_lib.attention_bias(q, k, v, bias, scale=1.0)
+    for b in range(B):
+        for h in range(H):
+            W = [[w * u ** i * int(C[b, h, i, j]) for j, (w, u) in enumerate(zip(wk, uk))] for i in range(nq)]
+            _check_exact(out[b, h], lse[b, h], W, vals[b][h])
+    assert np.all(out[0, 1, 2] == 0.0) and lse[0, 1, 2] == -math.inf
+    # a bias that is the same for every head is the shared mask
+    shared = np.broadcast_to(bias[:, :1], bias.shape).copy()
+    o2, l2 = oracle_lib.attention_bias(q, k, v, shared, scale=1.0)
+    o3, l3 = oracle_lib.attention(q, k, v, mask=bias[:, 0], scale=1.0)
+    np.testing.assert_array_equal(o2, o3)
+    np.testing.assert_array_equal(l2, l3)
+
+
 def test_closed_form_causal(oracle_lib):
     wk, uk = [1, 2, 3, 5], [3, 1, 2, 1]
     vals = [[2, 1], [-1, 4], [0, 0], [6, -6]]
