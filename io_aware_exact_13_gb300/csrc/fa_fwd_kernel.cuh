@@ -129,6 +129,7 @@ struct FwdParams {
     const int *cu_seqlens;  // [B + 1] token offsets of the sequences
     int total;              // tokens in the batch
     int Hkv;                // key/value heads
+    int rows_per_item;      // query rows per work item: 256 (two 128-row tiles) or 128 (one tile)
     int mask_tma;           // 1: the mask tensor map is valid (N % 4 == 0) and mask blocks arrive by TMA
     int mask_per_head;      // 1: the mask is a per-head bias [B][H][N][N]; 0: [B][N][N] shared by the heads
 };
@@ -150,7 +151,7 @@ __device__ __forceinline__ void item_coords(const FwdParams &p, int item, int &b
     const int BH = p.B * p.H;
     const int qb = p.n_qblk - 1 - item / BH;
     bh = item % BH;
-    q0 = qb * kRowsPerItem;
+    q0 = qb * p.rows_per_item;
 }
 
 // One work item as every role sees it: head row bh (= b*H + h), first query row
@@ -186,11 +187,11 @@ __device__ __forceinline__ int seq_len(const FwdParams &p, int s, int &a, bool &
     return bad ? 0 : b - a;
 }
 
-// Packed batch work list. A grid over nseq x H x ceil(max_seqlen / 256) slots
-// is mostly empty for short sequences, and empty slots unbalance the static
-// schedule. Instead the non-empty items form one compact list, longest first:
-// level l (query rows [256 l, 256 l + 256)) from the top level down, and within
-// a level every sequence longer than 256 l in index order, each with its H
+// Packed batch work list. A grid over nseq x H x ceil(max_seqlen / R) slots (R =
+// rows per item) is mostly empty for short sequences, and empty slots unbalance
+// the static schedule. Instead the non-empty items form one compact list, longest
+// first: level l (query rows [R l, R l + R)) from the top level down, and within
+// a level every sequence longer than R l in index order, each with its H
 // heads. A CTA takes list positions in the snake order of item_at. Positions
 // grow monotonically, so a cursor suffices: the current level, its first
 // position and sequence count, and a scan point (rank sequences of the level
@@ -200,7 +201,7 @@ struct VarlenCursor {
     int w = 0, lvl, cnt, start = 0, pos = 0, rank = 0;
 
     __device__ __forceinline__ static int count_level(const FwdParams &p, int l) {
-        const int thr = l * kRowsPerItem;
+        const int thr = l * p.rows_per_item;
         int c = 0;
         for (int s0 = 0; s0 < p.B; s0 += 32) {
             const int s = s0 + (int)(threadIdx.x & 31);
@@ -226,7 +227,7 @@ struct VarlenCursor {
         for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (__any_sync(0xffffffffu, any_bad) && blockIdx.x == 0 && (threadIdx.x & 31) == 0)
             atomicExch(p.status, kStatusSeqlens);
-        lvl = mx > 0 ? (mx - 1) / kRowsPerItem : -1;
+        lvl = mx > 0 ? (mx - 1) / p.rows_per_item : -1;
         cnt = lvl >= 0 ? count_level(p, lvl) : 0;
     }
 
@@ -245,7 +246,7 @@ struct VarlenCursor {
         }
         const int r = k - start;
         const int j = r / p.H, h = r - j * p.H;
-        const int thr = lvl * kRowsPerItem;
+        const int thr = lvl * p.rows_per_item;
         // the j-th sequence (0-based, index order) with rows at this level
         for (; pos < p.B; pos += 32) {
             const int s = pos + (int)(threadIdx.x & 31);

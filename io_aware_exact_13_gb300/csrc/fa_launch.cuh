@@ -84,6 +84,7 @@ int launch_variant(const LaunchArgs &a) {
     p.kv_group = a.H / a.Hkv;
     p.H = a.H;
     p.N = a.N;
+    p.rows_per_item = kRowsPerItem;
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
     p.n_kv = (a.N + kBK - 1) / kBK;
     split_tail(p, BH * p.n_qblk, a.num_sms, CAUSAL);
@@ -130,6 +131,7 @@ int launch_bk128(const LaunchArgs &a) {
     p.H = a.H;
     p.kv_group = a.H / a.Hkv;
     p.N = a.N;  // max_seqlen for a packed batch
+    p.rows_per_item = kRowsPerItem;
     p.n_qblk = (a.N + kRowsPerItem - 1) / kRowsPerItem;
     p.n_kv = (a.N + kBK128 - 1) / kBK128;
     if (VARLEN) {
