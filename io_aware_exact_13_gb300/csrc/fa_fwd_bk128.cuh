@@ -39,7 +39,7 @@
 //   warps 4-7   softmax + epilogue of query tile 1
 //   warp  8     TMA producer: Q tiles per item, then K and V rings
 //   warp  9     S issuer: S_t(j) = Q_t K_j^T for t = 0, 1 in turn, into the S buffer
-//   warps 10-11 P V issuer of tile t = warp - 10: O_t += P_t(j) V_j
+//   warps 10-11 P V issuer of tile t = warp - 10: O_t += P_t(j) V_j, issued after S_t(j+1)
 //   warp  12    packed batch only: publishes the CTA's work items (ItemRing)
 //   warps 13-15 idle (they complete the last warpgroup)
 // Shared memory holds no static variables: the abort word and the item ring
@@ -82,8 +82,8 @@ struct Cfg128 {
     static constexpr int SMEM_V = SMEM_K + RK * KV_TILE;
     static constexpr int SMEM_BAR = SMEM_V + RV * KV_TILE;
     // q_full[2] q_empty[2] k_full[RK] k_empty[RK] v_full[RV] v_empty[RV] s_full[2] s_free p_full[2]
-    // pv_done[2][2] drain
-    static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 9 + 1;
+    // pv_done[2][2] drain s_issued[2][2]
+    static constexpr int NUM_BARS = 4 + 2 * RK + 2 * RV + 9 + 1 + 4;
     static constexpr int SMEM_TMEM_SLOT = SMEM_BAR + ((NUM_BARS * 8 + 15) / 16) * 16;
     static constexpr int SMEM_RING = SMEM_TMEM_SLOT + 16;         // ItemRing (packed batches)
     static constexpr int SMEM_ABORT = SMEM_RING + 128;
@@ -117,6 +117,8 @@ struct Sync128 {
     __device__ __forceinline__ uint32_t p_full(int t) const { return at(B0 + 3 + t); }
     __device__ __forceinline__ uint32_t pv_done(int t, int b) const { return at(B0 + 5 + 2 * t + b); }
     __device__ __forceinline__ uint32_t drain() const { return at(B0 + 9); }
+    // S_t(g) issued (the S issuer's lane 0 arrives once its products are in the queue)
+    __device__ __forceinline__ uint32_t s_issued(int t, int b) const { return at(B0 + 10 + 2 * t + b); }
 };
 
 // Row maximum of 128 values: eight independent three-input chains, then a short tree.
@@ -165,6 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sy.pv_done(t, 1), 1);
         }
         mbar_init(sy.s_free(), kBQ);  // the warpgroup of the tile whose S the buffer holds
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(sy.s_issued(t, 0), 1);
+            mbar_init(sy.s_issued(t, 1), 1);
+        }
         for (int s = 0; s < RK; ++s) {  // a K slot is released by the S issuer
             mbar_init(sy.k_full(s), 1);
             mbar_init(sy.k_empty(s), 1);
@@ -291,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t KVT16 = C::KV_TILE >> 4;
             constexpr uint64_t QT16 = C::Q_TILE >> 4;
             uint32_t qcount[2] = {0, 0}, kpos = 0, s_issued = 0;
+            uint32_t sg[2] = {0, 0};  // S products of each tile so far
             bool ok = true;
             ItemIter<VARLEN> iter(p, abort_flag, ring);
             for (Item itm; ok && iter.next(p, itm, ok);) {
@@ -325,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_commit(sy.s_full(t), issue);
                         if (j == nt[t] - 1) tc_commit(sy.q_empty(t), issue);
+                        if (lane == 0) mbar_arrive(sy.s_issued(t, sg[t] & 1u));
+                        ++sg[t];
                     }
                     tc_commit(sy.k_empty(slot), issue);  // after the last product that reads K_j
                 }
@@ -358,6 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     ok = wait_warp(sy.p_full(t), pcount & 1u, abort_flag, p);
+                    // The tile's next S product goes into the tensor core's queue first: this product
+                    // is not on the critical path, S(j+1) is (the softmax waits for it).
+                    if (ok && j + 1 < nt)
+                        ok = wait_warp(sy.s_issued(t, (pcount + 1) & 1u), ((pcount + 1) >> 1) & 1u, abort_flag, p);
                     ++pcount;
                     if (!ok) break;
                     tc_fence_after();

@@ -415,7 +415,7 @@ def simulate_bwd_halves(n_it, stages, seed):
 
 
 def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0, s_waits_free=True,
-                   p_waits_pv=True, late_weight=1.0):
+                   p_waits_pv=True, late_weight=1.0, pv_after_next_s=True, s_issued_barriers=2):
     """The 128-key-block forward (fa_fwd_bk128_kernel) for one CTA: TMA producer,
     the S issuer (S_t(j) for t = 0, 1 in turn into the one S buffer), one P V
     issuer per tile, the eight softmax warps and (``item_ring`` > 0) the
@@ -434,9 +434,15 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
     further); a P V product counts as done for O only when its commit arrives,
     and the softmax may rescale or read O only after all earlier ones are done.
 
+    The P V issuer of tile t issues P V_t(j) only once the S issuer has issued
+    S_t(j+1) (when the item has one), so that P V products never queue ahead of a
+    pending S product; the S issuer signals each issue on s_issued{t}{g % 2}.
+
     Mutations that must be caught: ``s_waits_free=False`` (the S issuer does not
     wait for the S buffer to be copied out), ``p_waits_pv=False`` (the softmax
-    stores P_t(g) without waiting for P V_t(g-1), and rescales O without it)."""
+    stores P_t(g) without waiting for P V_t(g-1), and rescales O without it),
+    ``s_issued_barriers=1`` (one s_issued barrier per tile: the S issuer can run
+    two phases ahead of the P V issuer's wait)."""
     rnd = random.Random(seed)
     B = {}
     BK128 = 128
@@ -450,6 +456,9 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
                         ("pv_done1", 1)):
             bar(f"{name}{t}", c)
     bar("s_free", BQ)
+    for t in range(2):
+        for b in range(2):
+            bar(f"s_issued{t}{b}", 1)
     for s_ in range(rk):
         bar(f"k_full{s_}", 1)
         bar(f"k_empty{s_}", 1)
@@ -542,6 +551,8 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
                     issued += 1
                     tensor_pipe.extend([("mma", "S", t, g0[t] + j), ("commit", f"s_full{t}")]
                                        + ([("commit", f"q_empty{t}")] if j == n[t] - 1 else []))
+                    gi = g0[t] + j
+                    yield ("arrive", f"s_issued{t}{gi % s_issued_barriers}", 1)
                 tensor_pipe.append(("commit", f"k_empty{s_}"))
             for t in range(2):
                 g0[t] += n[t]
@@ -560,6 +571,9 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
                     yield ("arrive", f"v_empty{s_}", 1)
                     continue
                 yield ("wait", f"p_full{t}", pcount)
+                if pv_after_next_s and j + 1 < n[t]:  # S_t of the next block is issued first
+                    nxt = pcount + 1
+                    yield ("wait", f"s_issued{t}{nxt % s_issued_barriers}", nxt // s_issued_barriers)
                 tensor_pipe.extend([("mma", "PV", t, pcount), ("late", t, pcount), ("commit", f"v_empty{s_}")])
                 pcount += 1
         yield from take(len(items))

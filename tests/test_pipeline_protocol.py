@@ -152,11 +152,11 @@ def test_bk128_single_tile_units_and_packed_items():
         assert simulate_bk128(1000, True, single, 3, 2, seed)
 
 
-@pytest.mark.parametrize("mutation", [{"s_waits_free": False}, {"p_waits_pv": False}])
+@pytest.mark.parametrize("mutation", [{"s_waits_free": False}, {"p_waits_pv": False}, {"s_issued_barriers": 1}])
 def test_bk128_mutations_are_caught(mutation):
-    """An S issuer that does not wait for the S buffer to be copied out, and a softmax
-    that stores P (or rescales O) without waiting for the previous P V product: each
-    caught."""
+    """An S issuer that does not wait for the S buffer to be copied out, a softmax that
+    stores P (or rescales O) without waiting for the previous P V product, and one
+    s_issued barrier per tile instead of two (parity aliasing): each caught."""
     from pipeline_model import simulate_bk128
 
     caught = 0
