@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
     if (warp >= 8) {
-        setmaxnreg_dec<64>();
+        setmaxnreg_dec<72>();
         if (warp == 8) {
             // ---------------------------------------------------------- TMA producer
             // Load order per item: Q tiles, K_0, then K_{j+1}, V_j for j = 0 .. nmax-1
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        setmaxnreg_inc<192>();
+        setmaxnreg_inc<184>();
         // -------------------------------------------------------------- softmax + epilogue
         const int t = warp >> 2;  // query tile of this warpgroup
         const int r = threadIdx.x & 127;

@@ -106,10 +106,10 @@ int launch_bk128(const LaunchArgs &a) {
     using C = Cfg128<T, D>;
     auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN>;
     // The register split between warpgroups assumes 128 registers per thread at
-    // launch (512 x 128 = 256 x 192 + 256 x 64). Refuse to launch otherwise.
+    // launch (512 x 128 = 256 x 184 + 256 x 72). Refuse to launch otherwise.
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return -5;
-    if (attr.numRegs * kThreads < 256 * 192 + 256 * 64) return -5;
+    if (attr.numRegs * kThreads < 256 * 184 + 256 * 72) return -5;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return -5;
     CUtensorMap tq, tk, tv;
