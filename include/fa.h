@@ -117,6 +117,34 @@ int fa_fwd_bias(const void *q, const void *k, const void *v, const float *bias, 
 int fa_fwd_bias_fp16(const void *q, const void *k, const void *v, const float *bias, void *out, float *lse, int B,
                      int H, int N, int d, float scale, int causal, void *stream);
 
+/* ---- additive mask, packed -------------------------------------------------
+ * The forward of fa_fwd_gqa / fa_fwd_gqa_fp16 with a shared mask (required,
+ * float [B][N][N], 16-byte aligned) and a caller-owned DEVICE workspace
+ * (256-byte aligned, at least fa_fwd_masked_workspace_bytes(B, N) bytes; the
+ * call owns it until later work on `stream` starts). Hkv = H is multi-head
+ * attention.
+ * Most masks hold only 0 and -inf (padding, causal variants, sparsity
+ * patterns, fully masked rows), and for those the mask term of the glossary
+ * "FlashAttention", section "Move less data", is one bit per entry. Every call
+ * first reads the mask once and writes its one-bit form into the workspace
+ * (about B*N*N/8 bytes), with a verdict word. Then two kernels are queued:
+ * the 128-key-block kernel, which applies the bits, and the fp32-mask kernel
+ * of fa_fwd. Only the one that matches the verdict does any work. With a
+ * 0/-inf mask every head reads 16 bytes of bits per 128 keys instead of
+ * 512 bytes of fp32 mask. The results are those of the 128-key kernel
+ * without a mask, with masked keys excluded. A mask with any other value is
+ * applied as given, with the same results as fa_fwd. Errors as for fa_fwd;
+ * FA_ERR_NULL if mask is NULL, FA_ERR_WORKSPACE if the workspace is missing,
+ * misaligned or too small. fa_fwd_masked_workspace_bytes returns the size, or
+ * FA_ERR_SHAPE for B or N < 1. */
+long long fa_fwd_masked_workspace_bytes(int B, int N);
+int fa_fwd_masked(const void *q, const void *k, const void *v, const float *mask, void *out, float *lse, int B, int H,
+                  int Hkv, int N, int d, float scale, int causal, void *workspace, unsigned long long workspace_bytes,
+                  void *stream);
+int fa_fwd_masked_fp16(const void *q, const void *k, const void *v, const float *mask, void *out, float *lse, int B,
+                       int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
+                       unsigned long long workspace_bytes, void *stream);
+
 /* ---- split-KV forward for decoding ------------------------------------------
  * Same operation for Nq query rows (1 <= Nq <= 16) against Nk >= 1 keys:
  *   q, out : [B][H][Nq][d]      k, v : [B][H][Nk][d]      lse : float [B][H][Nq]

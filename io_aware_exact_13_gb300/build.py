@@ -1,6 +1,6 @@
 """Build ``libfa.so`` (the C-ABI CUDA library) in-tree with nvcc for sm_103a.
 
-One translation unit per element type plus the C ABI, compiled in parallel,
+A few translation units per element type plus the C ABI, compiled in parallel,
 then linked as a shared library next to this file. Only the CUDA runtime and
 the C++ standard library are linked; the driver entry point for tensor-map
 encoding is looked up at run time.
@@ -17,8 +17,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libfa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp16.cu", "fa_fwd_fp32.cu", "fa_splitkv.cu", "fa_splitkv_noalloc.cu",
-           "fa_bwd.cu", "fa_fwd_varlen_bf16.cu", "fa_fwd_varlen_fp16.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp16.cu", "fa_fwd_mask_bf16.cu", "fa_fwd_mask_fp16.cu",
+           "fa_mask_pack.cu", "fa_fwd_fp32.cu", "fa_splitkv.cu", "fa_splitkv_noalloc.cu", "fa_bwd.cu",
+           "fa_fwd_varlen_bf16.cu", "fa_fwd_varlen_fp16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", "-Wno-deprecated-gpu-targets"]

@@ -121,7 +121,7 @@ int check_args(Type ty, const void *q, const void *k, const void *v, const float
 
 int fwd_common(Type ty, const void *q, const void *k, const void *v, const float *mask, void *out, float *lse,
                int B, int H, int N, int d, float scale, int causal, void *stream, int Hkv = -1,
-               int mask_per_head = 0) {
+               int mask_per_head = 0, void *workspace = nullptr) {
     int rc = check_args(ty, q, k, v, mask, out, lse, B, H, N, d);
     if (rc != FA_OK) return rc;
     if (Hkv == -1) Hkv = H;
@@ -151,12 +151,37 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
     a.num_sms = di->num_sms;
     a.timeout_ns = kDefaultTimeoutNs;
     a.mask_per_head = mask_per_head;
+    // With a workspace, a shared mask is first packed to one bit per entry (on every call: the mask
+    // may change between calls); without one the fp32 mask is applied as given.
+    if (workspace && mask && !mask_per_head && ty != Type::FP32) {
+        const long long rows = static_cast<long long>(B) * N;
+        int *kind = reinterpret_cast<int *>(static_cast<char *>(workspace) + fa::mask_bits_bytes(rows, N));
+        if (fa::launch_mask_pack(mask, workspace, kind, rows, N, di->num_sms, a.stream) != 0) return FA_ERR_LAUNCH;
+        a.mask_bits = workspace;
+        a.mask_kind = kind;
+    }
     switch (ty) {
         case Type::BF16: rc = fa::launch_fwd_bf16(a); break;
         case Type::FP16: rc = fa::launch_fwd_fp16(a); break;
         case Type::FP32: rc = fa::launch_fwd_fp32(a); break;
     }
     return rc;
+}
+
+// bytes of the masked forward's workspace: the packed mask, then the packing pass's verdict word
+size_t masked_workspace_bytes(int B, int N) {
+    return fa::mask_bits_bytes(static_cast<long long>(B) * N, N) + 256;
+}
+
+int masked_common(Type ty, const void *q, const void *k, const void *v, const float *mask, void *out, float *lse,
+                  int B, int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
+                  unsigned long long workspace_bytes, void *stream) {
+    if (!mask) return FA_ERR_NULL;
+    int rc = check_args(ty, q, k, v, mask, out, lse, B, H, N, d);
+    if (rc != FA_OK) return rc;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < masked_workspace_bytes(B, N))
+        return FA_ERR_WORKSPACE;
+    return fwd_common(ty, q, k, v, mask, out, lse, B, H, N, d, scale, causal, stream, Hkv, 0, workspace);
 }
 
 // Forward from host buffers: the B*H head slabs are cut into n_chunks contiguous
@@ -452,6 +477,25 @@ int fa_fwd(const void *q, const void *k, const void *v, const float *mask_or_nul
 int fa_fwd_fp16(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
                 int B, int H, int N, int d, float scale, int causal, void *stream) {
     return fwd_common(Type::FP16, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
+}
+
+long long fa_fwd_masked_workspace_bytes(int B, int N) {
+    if (B < 1 || N < 1) return FA_ERR_SHAPE;
+    return static_cast<long long>(masked_workspace_bytes(B, N));
+}
+
+int fa_fwd_masked(const void *q, const void *k, const void *v, const float *mask, void *out, float *lse, int B, int H,
+                  int Hkv, int N, int d, float scale, int causal, void *workspace, unsigned long long workspace_bytes,
+                  void *stream) {
+    return masked_common(Type::BF16, q, k, v, mask, out, lse, B, H, Hkv, N, d, scale, causal, workspace,
+                         workspace_bytes, stream);
+}
+
+int fa_fwd_masked_fp16(const void *q, const void *k, const void *v, const float *mask, void *out, float *lse, int B,
+                       int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
+                       unsigned long long workspace_bytes, void *stream) {
+    return masked_common(Type::FP16, q, k, v, mask, out, lse, B, H, Hkv, N, d, scale, causal, workspace,
+                         workspace_bytes, stream);
 }
 
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,

@@ -1,5 +1,5 @@
-// fa_fwd_bk128.cuh -- the exact tiled attention forward with 128-key K/V blocks
-// (no additive mask), for sm_103a.
+// fa_fwd_bk128.cuh -- the exact tiled attention forward with 128-key K/V blocks,
+// for sm_103a (no mask, or a mask of 0 and -inf entries in its one-bit form).
 //
 // Same computation as fa_fwd_kernel.cuh ("FlashAttention: Exact Attention as an
 // IO-Aware Streaming Computation", sections "Core idea" and "Mathematical
@@ -136,12 +136,21 @@ __device__ __forceinline__ float row_max128(const float (&x)[128]) {
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
-template <typename T, int D, bool CAUSAL, bool VARLEN>
+// MASK: an additive [B][N][N] mask whose entries are all 0 or -inf, in its packed form
+// (p.mask_bits, one bit per entry, set = -inf; see fa_mask_pack.cu). Thread r reads the 16
+// bytes of its row and key block from global memory (L2: the packed mask of a batch index is
+// shared by its heads), one block ahead of its use.
+template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bk128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    static_assert(!(VARLEN && MASK), "no mask in a packed batch");
     using C = Cfg128<T, D>;
     constexpr int RK = C::RK, RV = C::RV;
+    if constexpr (MASK) {  // the mask had other values: the 64-key kernel applies it as given
+        if (*p.mask_kind != 0) return;
+        grid_launch_dependents();  // that kernel (queued next) may take the SMs this grid leaves idle
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (uint32_t)((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     if (pad > (uint32_t)C::SLACK) {  // cannot happen with no static shared memory; never overflow
@@ -427,6 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = q0 + t * kBQ + r;  // query row within the sequence (may be >= n in a ragged tail)
             const int tile_row0 = q0 + t * kBQ;
             float m_ref = -INFINITY, l = 0.0f;
+            // packed mask: this row's 16-byte units (a row past the end reads row 0; its output is not stored)
+            const uint4 *bits_row = nullptr;
+            uint4 bits = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (MASK) {
+                bits_row = p.mask_bits +
+                           ((size_t)(bh / p.H) * p.N + (size_t)(row < n ? row : 0)) * (size_t)p.mask_bits_blk;
+                bits = __ldg(bits_row);
+            }
             for (int j = 0; j < nt; ++j, ++g) {
                 ok = wait_warp(sy.s_full(t), scount & 1u, abort_flag, p);
                 ++scount;
@@ -446,6 +463,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(sy.s_free());  // the S buffer may now take the next product
+                if constexpr (MASK) {
+                    // bit e of word c is key 4 e + c of the block; the next block's bits are loaded now
+                    const uint4 nb = (j + 1 < nt) ? __ldg(bits_row + j + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t w[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[4 * e + c] = ((w[c] >> e) & 1u) ? -INFINITY : x[4 * e + c];
+                    }
+                    bits = nb;
+                }
                 // keys past the end of the sequence, and (causal) keys after the query
                 const int kbase = j * kBK128;
                 const bool ragged = kbase + kBK128 > n;

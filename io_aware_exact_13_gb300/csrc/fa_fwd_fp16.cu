@@ -1,14 +1,10 @@
-// fp16 instantiations of the forward: the 128-key-block kernel without a mask,
-// the 64-key-block kernel with an additive mask.
+// fp16 instantiations of the forward without a mask (the 128-key-block kernel);
+// a forward with a mask goes to fa_fwd_mask_fp16.cu.
 #include "fa_launch.cuh"
 
 namespace fa {
 int launch_fwd_fp16(const LaunchArgs &a) {
-    if (a.mask) {
-        if (a.d == 128) return launch_masked_d<__half, 128>(a);
-        if (a.d == 64) return launch_masked_d<__half, 64>(a);
-        return -4;
-    }
+    if (a.mask) return launch_fwd_mask_fp16(a);
     if (a.d == 128) return launch_bk128_d<__half, 128, false>(a);
     if (a.d == 64) return launch_bk128_d<__half, 64, false>(a);
     return -4;

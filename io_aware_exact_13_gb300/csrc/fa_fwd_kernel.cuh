@@ -49,6 +49,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -132,6 +133,13 @@ struct FwdParams {
     int rows_per_item;      // query rows per work item: 256 (two 128-row tiles) or 128 (one tile)
     int mask_tma;           // 1: the mask tensor map is valid (N % 4 == 0) and mask blocks arrive by TMA
     int mask_per_head;      // 1: the mask is a per-head bias [B][H][N][N]; 0: [B][N][N] shared by the heads
+    // A [B][N][N] mask packed to one bit per entry (fa_mask_pack.cu): [B][N][mask_bits_blk] 16-byte units,
+    // or nullptr. mask_kind is the packing pass's verdict, read at kernel start: 0 = every entry was 0 or
+    // -inf (the 128-key kernel applies the bits), 1 = some other value (the 64-key kernel applies the fp32
+    // mask). Each of the two kernels returns at once when the verdict is the other one's.
+    const uint4 *mask_bits;
+    int mask_bits_blk;
+    const int *mask_kind;
 };
 
 // Static schedule: CTA c takes item w*G + c in even waves w and w*G + (G-1-c)
@@ -432,6 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(!(VARLEN && HAS_MASK), "no mask in a packed batch");
     using C = Cfg<T, D, HAS_MASK>;
     constexpr int R = C::RING;
+    if constexpr (HAS_MASK) {
+        if (p.mask_kind != nullptr) {
+            // queued behind the 128-key kernel as its programmatic dependent: let that grid finish
+            // (so that later work on the stream is ordered after it), then return if it applied the mask
+            grid_dependency_wait();
+            if (*p.mask_kind == 0) return;
+        }
+    }
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Sync<R> sy{reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR)};

@@ -27,7 +27,17 @@ struct LaunchArgs {
     const int *cu_seqlens = nullptr;
     int total = 0;
     int mask_per_head = 0;  // the mask is a per-head bias [B][H][N][N]
+    // the shared mask packed to one bit per entry, and the packing pass's verdict (fa_mask_pack.cu);
+    // nullptr: the fp32 mask is applied as given
+    const void *mask_bits = nullptr;
+    const int *mask_kind = nullptr;
 };
+
+// Defined in fa_mask_pack.cu: bytes of the packed form of a [rows][nk] mask, and the packing pass
+// (zeroes *kind, then sets it to 1 if some entry is neither 0 nor -inf). Returns 0 or -5.
+size_t mask_bits_bytes(long long rows, int nk);
+int launch_mask_pack(const float *mask, void *bits, int *kind, long long rows, int nk, int num_sms,
+                     cudaStream_t stream);
 
 // Defined in fa_api.cu: encodes a [B*H][N][d] tensor map with box_rows-row x
 // 128-byte boxes and 128-byte swizzle. Returns false on failure.
@@ -95,16 +105,27 @@ int launch_variant(const LaunchArgs &a) {
     p.Hkv = a.Hkv;
     p.mask_tma = mask_tma ? 1 : 0;
     p.mask_per_head = a.mask_per_head;
+    p.mask_bits = nullptr;
+    p.mask_bits_blk = 0;
+    p.mask_kind = MASK ? a.mask_kind : nullptr;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
+    if (MASK && a.mask_kind != nullptr)  // behind the 128-key kernel on the packed mask (see launch_mask_fwd_d)
+        return launch_dependent(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, a.stream, tq, tk, tv, tm, p) ==
+                       cudaSuccess
+                   ? 0
+                   : -5;
     kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tm, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
-// The 128-key-block kernel (no mask): dense [B][H][N][d] tensors, or a packed batch.
-template <typename T, int D, bool CAUSAL, bool VARLEN>
+// The 128-key-block kernel: dense [B][H][N][d] tensors, or a packed batch; MASK: a shared
+// [B][N][N] mask in its packed one-bit form.
+template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false>
 int launch_bk128(const LaunchArgs &a) {
+    static_assert(!(VARLEN && MASK), "no mask in a packed batch");
     using C = Cfg128<T, D>;
-    auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN>;
+    auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN, MASK>;
+    if (MASK && (a.mask_bits == nullptr || a.mask_kind == nullptr)) return -5;
     // The register split between warpgroups assumes 128 registers per thread at
     // launch (512 x 128 = 256 x 184 + 256 x 72). Refuse to launch otherwise.
     cudaFuncAttributes attr;
@@ -146,6 +167,10 @@ int launch_bk128(const LaunchArgs &a) {
     p.total = VARLEN ? a.total : 0;
     p.Hkv = a.Hkv;
     p.mask_tma = 0;
+    p.mask_per_head = 0;
+    p.mask_bits = MASK ? static_cast<const uint4 *>(a.mask_bits) : nullptr;
+    p.mask_bits_blk = MASK ? (a.N + kBK128 - 1) / kBK128 : 0;
+    p.mask_kind = MASK ? a.mask_kind : nullptr;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
@@ -161,5 +186,22 @@ template <typename T, int D>
 int launch_masked_d(const LaunchArgs &a) {
     return a.causal ? launch_variant<T, D, true, true>(a) : launch_variant<T, D, false, true>(a);
 }
+
+// A forward with an additive mask. With the packed form of a shared mask, both kernels are queued:
+// the 128-key kernel applies the bits when every entry was 0 or -inf, the 64-key kernel the fp32
+// mask otherwise, and each returns at once when the verdict is the other one's. The 64-key kernel
+// is the 128-key kernel's programmatic dependent: when it only has to return, its CTAs do so on the
+// SMs the 128-key grid's last wave leaves idle, after waiting for that grid to finish.
+template <typename T, int D>
+int launch_mask_fwd_d(const LaunchArgs &a) {
+    if (a.mask_bits != nullptr && a.mask_kind != nullptr && !a.mask_per_head) {
+        const int rc = a.causal ? launch_bk128<T, D, true, false, true>(a) : launch_bk128<T, D, false, false, true>(a);
+        if (rc != 0) return rc;
+    }
+    return launch_masked_d<T, D>(a);
+}
+
+int launch_fwd_mask_bf16(const LaunchArgs &a);  // fa_fwd_mask_bf16.cu
+int launch_fwd_mask_fp16(const LaunchArgs &a);  // fa_fwd_mask_fp16.cu
 
 }  // namespace fa

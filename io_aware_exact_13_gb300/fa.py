@@ -6,6 +6,7 @@ There is no CPU fallback: importing this module fails loudly when the library
 has not been built, and every call raises if the library returns an error.
 
 Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
+``fa_fwd_masked`` / ``fa_fwd_masked_fp16`` (a shared mask packed in a workspace),
 ``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), ``fa_bwd`` /
 ``fa_bwd_fp16`` (backward by recomputation), ``fa_fwd_varlen`` /
 ``fa_fwd_varlen_fp16`` (packed variable-length batches), their sizing helpers,
@@ -52,6 +53,11 @@ SIGNATURES = {
     "fa_fwd_bias": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_bias_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_gqa": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
+    "fa_fwd_masked_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 2),
+    "fa_fwd_masked": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp,
+                                                                        ctypes.c_ulonglong, _vp]),
+    "fa_fwd_masked_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp,
+                                                                             ctypes.c_ulonglong, _vp]),
     "fa_fwd_gqa_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_splitkv_num_splits": (ctypes.c_int, [ctypes.c_int] * 5),
     "fa_splitkv_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 5),
@@ -143,15 +149,66 @@ _BY_DTYPE = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_fp16, torch.float32: 
 
 
 def attention(q, k, v, mask=None, scale=None, causal=False, out=None, lse=None, stream=None):
-    """O, lse = softmax(scale * q k^T + mask) v for [B,H,N,d] CUDA tensors."""
+    """O, lse = softmax(scale * q k^T + mask) v for [B,H,N,d] CUDA tensors. A bf16 / fp16
+    forward with a mask goes through ``fa_fwd_masked`` with a workspace from torch."""
     if q.dtype not in _BY_DTYPE:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
+    if mask is not None and q.dtype in _MASKED:
+        ws = torch.empty(fa_fwd_masked_workspace_bytes(B, N), dtype=torch.uint8, device=q.device)
+        _MASKED[q.dtype](q, k, v, mask, out, lse, scale, causal, ws, stream)
+    else:
+        _BY_DTYPE[q.dtype](q, k, v, mask, out, lse, scale, causal, stream)
     return out, lse
+
+
+# ---------------------------------------------------------------- additive mask, packed
+def fa_fwd_masked_workspace_bytes(B, N) -> int:
+    n = int(lib.fa_fwd_masked_workspace_bytes(int(B), int(N)))
+    if n < 0:
+        raise FAError(n, "fa_fwd_masked_workspace_bytes")
+    return n
+
+
+def _fwd_masked(fn_name, dtype, q, k, v, mask, out, lse, scale, causal, workspace, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape or out.shape != q.shape or H % Hkv:
+        raise ValueError("q, out: [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, N] tensor")
+    if (mask is None or mask.dtype != torch.float32 or mask.shape != (B, N, N) or not mask.is_contiguous()
+            or not mask.is_cuda):
+        raise ValueError("mask must be a contiguous CUDA float32 [B, N, N] tensor")
+    if workspace is None or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                               float(scale), int(bool(causal)), _ptr(workspace), nbytes,
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_masked(q, k, v, mask, out, lse, scale, causal, workspace, stream=None):
+    """bf16 forward with a shared [B, N, N] fp32 mask, packed to one bit per entry in ``workspace``
+    (at least ``fa_fwd_masked_workspace_bytes(B, N)`` bytes) when its entries are all 0 or -inf;
+    k, v may hold fewer heads (grouped-query)."""
+    _fwd_masked("fa_fwd_masked", torch.bfloat16, q, k, v, mask, out, lse, scale, causal, workspace, stream)
+
+
+def fa_fwd_masked_fp16(q, k, v, mask, out, lse, scale, causal, workspace, stream=None):
+    """fp16 forward with a shared mask and a workspace (see ``fa_fwd_masked``)."""
+    _fwd_masked("fa_fwd_masked_fp16", torch.float16, q, k, v, mask, out, lse, scale, causal, workspace, stream)
+
+
+_MASKED = {torch.bfloat16: fa_fwd_masked, torch.float16: fa_fwd_masked_fp16}
 
 
 # ---------------------------------------------------------------- forward from host memory

@@ -226,3 +226,33 @@ def test_host_forward_validation(fa, name):
     assert call(chunks=0) == fa.FA_ERR_SHAPE
     assert call(chunks=3) == fa.FA_ERR_SHAPE  # more chunks than B*H = 2
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ["fa_fwd_masked", "fa_fwd_masked_fp16"])
+def test_masked_host_validation(fa, name):
+    f = getattr(fa.lib, name)
+    need = fa.fa_fwd_masked_workspace_bytes(2, 300)
+
+    def call(mask=0x60000, H=4, Hkv=2, N=300, d=128, ws=0x100000, ws_bytes=None):
+        return f(ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000),
+                 ctypes.c_void_p(mask) if mask else None, ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000),
+                 2, H, Hkv, N, d, ctypes.c_float(0.1), 0, ctypes.c_void_p(ws) if ws else None,
+                 need if ws_bytes is None else ws_bytes, None)
+
+    assert call(mask=0) == fa.FA_ERR_NULL       # the mask is required
+    assert call(mask=0x60004) == fa.FA_ERR_ALIGN
+    assert call(N=0) == fa.FA_ERR_SHAPE
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(ws=0) == fa.FA_ERR_WORKSPACE
+    assert call(ws=0x100010) == fa.FA_ERR_WORKSPACE  # not 256-byte aligned
+    assert call(ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert call(Hkv=3) == fa.FA_ERR_SHAPE            # Hkv must divide H
+
+
+def test_masked_workspace_size(fa):
+    # one bit per (row, key) in 16-byte units of 128 keys, then 256 bytes for the verdict word
+    assert fa.fa_fwd_masked_workspace_bytes(2, 4096) == 2 * 4096 * 32 * 16 + 256
+    assert fa.fa_fwd_masked_workspace_bytes(1, 1) == 16 + 256
+    assert fa.fa_fwd_masked_workspace_bytes(3, 129) == 3 * 129 * 2 * 16 + 256
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_masked_workspace_bytes(0, 16)
