@@ -18,7 +18,10 @@ Pins (what ties each routine to the pages rather than to itself) are in
   "Why a tile can be discarded", "One row, checked two ways" and "Practice":
   block summaries, their merge and the two worked examples.
 * "IO-aware exact attention", sections "Tile order and on-chip capacity"
-  (causal: keys at or before the query) and "Backward recomputation".
+  (causal: keys at or before the query), "Backward recomputation" and "Why
+  implementations form a family" (bias and dropout as variants).
+* Dropout's keep decisions: the counter-based generator Philox4x64-10 of Salmon,
+  Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011).
 """
 from __future__ import annotations
 
@@ -69,8 +72,15 @@ def _load():
     lib.oracle_block_summary_f64.restype = None
     lib.oracle_merge_f64.argtypes = [ctypes.c_double, ctypes.c_double, dp, ctypes.c_double, ctypes.c_double, dp, i64, dp, dp, dp]
     lib.oracle_merge_f64.restype = None
+    u64 = ctypes.c_uint64
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.oracle_philox4x64_10.argtypes = [u64p, u64p, u64p]
+    lib.oracle_philox4x64_10.restype = None
+    lib.oracle_dropout_keep.argtypes = [ctypes.POINTER(ctypes.c_uint8), i64, i64, i64, i64, ctypes.c_int, u64, u64]
+    lib.oracle_attn_dropout_f64.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64, i64, ctypes.c_double,
+                                            ctypes.c_int, ctypes.c_int, u64, u64]
     for f in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_blockwise_f64, lib.oracle_attn_bwd_f64,
-              lib.oracle_num_threads):
+              lib.oracle_num_threads, lib.oracle_dropout_keep, lib.oracle_attn_dropout_f64):
         f.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -211,3 +221,49 @@ def attention_bwd(q, k, v, dout, mask=None, scale=None, causal=False):
     if rc != 0:
         raise RuntimeError("oracle_attn_bwd_f64 failed")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- dropout
+def dropout_threshold(p_drop: float) -> int:
+    """Keep threshold of drop probability p: the keep probability (1 - p) rounded to a
+    multiple of 1/256 (halves up), as a count of the 256 byte values that keep."""
+    t = int(np.floor((1.0 - float(p_drop)) * 256.0 + 0.5))
+    if not 1 <= t <= 256:
+        raise ValueError(f"drop probability {p_drop} keeps nothing (or is negative)")
+    return t
+
+
+def philox4x64_10(counter, key):
+    """One Philox4x64-10 block (Salmon et al., SC 2011): four 64-bit words."""
+    c = (ctypes.c_uint64 * 4)(*[int(x) & (2**64 - 1) for x in counter])
+    k = (ctypes.c_uint64 * 2)(*[int(x) & (2**64 - 1) for x in key])
+    o = (ctypes.c_uint64 * 4)()
+    _load().oracle_philox4x64_10(c, k, o)
+    return tuple(int(x) for x in o)
+
+
+def dropout_keep(B, H, Nq, Nk, p_drop, seed, offset=0):
+    """keep[B, H, Nq, Nk] (bool) of the dropout definition in attn_oracle.h."""
+    keep = np.zeros((B, H, Nq, Nk), dtype=np.uint8)
+    rc = _load().oracle_dropout_keep(keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), B, H, Nq, Nk,
+                                     dropout_threshold(p_drop), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1))
+    if rc != 0:
+        raise RuntimeError("oracle_dropout_keep failed")
+    return keep.astype(bool)
+
+
+def attention_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False):
+    """fp64 attention with dropout ("IO-aware exact attention", section "Why
+    implementations form a family", names the variant; the reading and the keep
+    stream are stated in attn_oracle.h). Returns (out [B,H,Nq,d], lse [B,H,Nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, Nk, d = _shapes(q, k, v, None)
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    out = np.zeros((B, H, Nq, d))
+    lse = np.zeros((B, H, Nq))
+    rc = _load().oracle_attn_dropout_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d, scale,
+                                         int(bool(causal)), dropout_threshold(p_drop), int(seed) & (2**64 - 1),
+                                         int(offset) & (2**64 - 1))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_dropout_f64 failed")
+    return out, lse

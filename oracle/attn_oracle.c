@@ -273,3 +273,115 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
     }
     return err ? -1 : 0;
 }
+
+/* ---- dropout (see attn_oracle.h) ---------------------------------------------
+ * Philox4x64-10 (Salmon et al., SC 2011): a round multiplies counter words 0 and
+ * 2 by the two multipliers, and the new counter is (hi(M1 x2) ^ x1 ^ k0,
+ * lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0)); the key is bumped by the two Weyl
+ * constants (the golden ratio and sqrt(3) - 1 in 64-bit fixed point) after
+ * every round. */
+static const uint64_t PHILOX_M0 = 0xD2E7470EE14C6C93ull;
+static const uint64_t PHILOX_M1 = 0xCA5A826395121157ull;
+static const uint64_t PHILOX_W0 = 0x9E3779B97F4A7C15ull;
+static const uint64_t PHILOX_W1 = 0xBB67AE8584CAA73Bull;
+
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        const unsigned __int128 p0 = (unsigned __int128)PHILOX_M0 * x0;
+        const unsigned __int128 p1 = (unsigned __int128)PHILOX_M1 * x2;
+        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        x0 = hi1 ^ x1 ^ k0;
+        x1 = lo1;
+        x2 = hi0 ^ x3 ^ k1;
+        x3 = lo0;
+        k0 += PHILOX_W0;
+        k1 += PHILOX_W1;
+    }
+    out[0] = x0;
+    out[1] = x1;
+    out[2] = x2;
+    out[3] = x3;
+}
+
+/* keep decisions of row (b, h, i) for keys 0 .. Nk-1 */
+static void keep_row(uint8_t *keep, int64_t H, int64_t Nk, int threshold, uint64_t seed, uint64_t offset,
+                     int64_t b, int64_t h, int64_t i) {
+    const uint64_t key[2] = {seed, 0};
+    for (int64_t g = 0; g * 32 < Nk; ++g) {
+        const uint64_t ctr[4] = {(uint64_t)i, (uint64_t)g, (uint64_t)(b * H + h), offset};
+        uint64_t w[4];
+        oracle_philox4x64_10(ctr, key, w);
+        for (int64_t t = 0; t < 32 && g * 32 + t < Nk; ++t) {
+            const unsigned byte = (unsigned)((w[t / 8] >> (8 * (t % 8))) & 0xFFu);
+            keep[g * 32 + t] = byte < (unsigned)threshold ? 1 : 0;
+        }
+    }
+}
+
+int oracle_dropout_keep(uint8_t *keep, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int threshold,
+                        uint64_t seed, uint64_t offset) {
+    if (!keep || B < 0 || H < 0 || Nq < 0 || Nk < 0 || threshold < 1 || threshold > 256) return -1;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int64_t row = 0; row < B * H * Nq; ++row) {
+        const int64_t i = row % Nq, bh = row / Nq;
+        keep_row(keep + row * Nk, H, Nk, threshold, seed, offset, bh / H, bh % H, i);
+    }
+    return 0;
+}
+
+/* Softmax over the materialised row s, as attend_row; then each kept key's
+ * probability, scaled by 1/q, weights its value row. */
+static void attend_row_dropout(const double *v, int64_t H, int64_t Nk, int64_t d, int64_t b, int64_t h,
+                               const double *s, const uint8_t *keep, double inv_q, double *o, double *lse) {
+    const double *vb = v + (b * H + h) * Nk * d;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Nk; ++j)
+        if (s[j] > m) m = s[j];
+    for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+    if (m == -INFINITY) {
+        *lse = -INFINITY;
+        return;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        double p = exp(s[j] - m);
+        if (p == 0.0) continue;
+        l += p;
+        if (keep[j])
+            for (int64_t t = 0; t < d; ++t) o[t] += p * vb[j * d + t];
+    }
+    for (int64_t t = 0; t < d; ++t) o[t] = (o[t] / l) * inv_q;
+    *lse = m + log(l);
+}
+
+int oracle_attn_dropout_f64(const double *q, const double *k, const double *v, double *out, double *lse,
+                            int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale,
+                            int causal, int threshold, uint64_t seed, uint64_t offset) {
+    if (bad_args(q, k, v, B, H, Nq, Nk, d) || !out || !lse || threshold < 1 || threshold > 256) return -1;
+    const double inv_q = 256.0 / (double)threshold;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        uint8_t *keep = (uint8_t *)malloc((size_t)(Nk > 0 ? Nk : 1));
+        if (!s || !keep) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t row = 0; row < B * H * Nq; ++row) {
+            if (!s || !keep) continue;
+            const int64_t i = row % Nq, bh = row / Nq;
+            const int64_t b = bh / H, h = bh % H;
+            score_row(q, k, NULL, H, Nq, Nk, d, scale, causal, b, h, i, s);
+            keep_row(keep, H, Nk, threshold, seed, offset, b, h, i);
+            attend_row_dropout(v, H, Nk, d, b, h, s, keep, inv_q, out + row * d, lse + row);
+        }
+        free(s);
+        free(keep);
+    }
+    return err ? -1 : 0;
+}

@@ -65,6 +65,33 @@ int oracle_attn_bwd_f64(const double *q, const double *k, const double *v, const
 /* Number of OpenMP threads the routines above use. */
 int oracle_num_threads(void);
 
+/* ---- dropout ---------------------------------------------------------------
+ * [Lesson] "Why implementations form a family" names dropout as one of the
+ * variants that modify the calculation and defines nothing further. Reading
+ * used (the usual one for attention): the normalised probabilities P_ij are
+ * multiplied by keep_ij / q before the weighted sum over V; lse stays that of
+ * the undropped scores. The keep probability is q = threshold / 256
+ * (1 <= threshold <= 256) and keep_ij = [u_ij < threshold] for a byte u_ij of a
+ * counter-based stream:
+ *   u_ij = byte (j mod 32) of Philox4x64-10(counter = {i, j div 32, b*H + h, offset},
+ *                                            key = {seed, 0}),
+ * bytes numbered from the least significant byte of output word 0 upward
+ * (word j mod 32 div 8, bits 8 * (j mod 8) ...).
+ * Philox4x64-10 is the generator of Salmon, Moraes, Dror and Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3" (SC 2011). */
+
+/* One Philox4x64-10 block: out = the 256-bit image of the counter under the key. */
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+
+/* keep[B][H][Nq][Nk] (0 or 1) as defined above. Returns 0, or -1 on a bad argument. */
+int oracle_dropout_keep(uint8_t *keep, int64_t B, int64_t H, int64_t Nq, int64_t Nk, int threshold,
+                        uint64_t seed, uint64_t offset);
+
+/* Attention with dropout (no mask; causal as above). Returns 0, or -1 on a bad argument. */
+int oracle_attn_dropout_f64(const double *q, const double *k, const double *v, double *out, double *lse,
+                            int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, double scale,
+                            int causal, int threshold, uint64_t seed, uint64_t offset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,14 @@ MUTANTS = [
     ("bwd_drops_D", "double dsij = pij * (dp[j] - rowdot);", "double dsij = pij * dp[j];"),
     ("bwd_dk_unscaled", "dkb[j * d + t] += scale * dsij * qi[t];", "dkb[j * d + t] += dsij * qi[t];"),
     ("bwd_dv_uses_dp", "dvb[j * d + t] += pij * doi[t];", "dvb[j * d + t] += dp[j] * doi[t];"),
+    ("philox_nine_rounds", "for (int round = 0; round < 10; ++round) {", "for (int round = 0; round < 9; ++round) {"),
+    ("philox_words_swapped", "        x0 = hi1 ^ x1 ^ k0;\n", "        x0 = hi0 ^ x1 ^ k0;\n"),
+    ("dropout_counter_order", "const uint64_t ctr[4] = {(uint64_t)i, (uint64_t)g, (uint64_t)(b * H + h), offset};",
+     "const uint64_t ctr[4] = {(uint64_t)g, (uint64_t)i, (uint64_t)(b * H + h), offset};"),
+    ("dropout_byte_order", "const unsigned byte = (unsigned)((w[t / 8] >> (8 * (t % 8))) & 0xFFu);",
+     "const unsigned byte = (unsigned)((w[t % 4] >> (8 * (t / 4))) & 0xFFu);"),
+    ("dropout_renormalised", "        l += p;\n        if (keep[j])", "        if (keep[j]) l += p;\n        if (keep[j])"),
+    ("dropout_unscaled", "o[t] = (o[t] / l) * inv_q;", "o[t] = o[t] / l;"),
 ]
 
 

@@ -412,3 +412,107 @@ def test_rejects_bad_shapes(oracle_lib):
         oracle_lib.attention(q, np.zeros((1, 1, 4, 4)), np.zeros((1, 1, 4, 4)))
     with pytest.raises(ValueError):
         oracle_lib.attention(q, q, q, mask=np.zeros((1, 4, 5)))
+
+
+# ---------------------------------------------------------------- dropout
+# The keep stream is Philox4x64-10 (Salmon et al., SC 2011); numpy's Philox bit
+# generator is an independent implementation of the same published algorithm. It
+# advances its counter once before producing a block, so its output for counter c is
+# the block of counter c + 1.
+
+@pytest.mark.parametrize("counter,key", [
+    ([0, 0, 0, 0], [0, 0]),
+    ([7, 11, 13, 17], [3, 5]),
+    ([2**64 - 2, 2**64 - 1, 5, 2**63], [2**64 - 1, 12345]),  # carry out of word 0 into word 1
+    ([123456789, 0, 42, 9], [0xDEADBEEF, 0]),
+])
+def test_philox_matches_numpy(oracle_lib, counter, key):
+    assert list(oracle_lib.philox4x64_10(counter, key)) == _numpy_philox_block(counter, key)
+
+
+def _as_int(words):
+    return sum(int(w) << (64 * n) for n, w in enumerate(words))
+
+
+def _numpy_philox_block(counter, key):
+    """numpy's Philox output for the block at `counter` (it steps the 256-bit counter by
+    one first; counter and key are passed as Python integers, which numpy takes exactly)."""
+    bg = np.random.Philox(key=_as_int(key), counter=(_as_int(counter) - 1) % 2**256)
+    return [int(x) for x in bg.random_raw(4)]
+
+
+def test_dropout_keep_stream_through_numpy(oracle_lib):
+    """Every keep decision of a small problem, recomputed from numpy's Philox with the
+    stated counter layout {i, j div 32, b*H + h, offset}, key {seed, 0}, bytes from
+    the low byte of word 0 upward."""
+    B, H, Nq, Nk, p, seed, offset = 2, 3, 5, 70, 0.3, 987654321, 17
+    keep = oracle_lib.dropout_keep(B, H, Nq, Nk, p, seed, offset)
+    t = oracle_lib.dropout_threshold(p)
+    assert t == 179  # 0.7 * 256 = 179.2
+    for b in range(B):
+        for h in range(H):
+            for i in range(Nq):
+                for g in range((Nk + 31) // 32):
+                    words = _numpy_philox_block([i, g, b * H + h, offset], [seed, 0])
+                    for tt in range(min(32, Nk - 32 * g)):
+                        byte = (words[tt // 8] >> (8 * (tt % 8))) & 0xFF
+                        assert keep[b, h, i, 32 * g + tt] == (byte < t), (b, h, i, g, tt)
+
+
+def test_dropout_threshold_rounding(oracle_lib):
+    assert oracle_lib.dropout_threshold(0.0) == 256
+    assert oracle_lib.dropout_threshold(0.5) == 128
+    assert oracle_lib.dropout_threshold(0.1) == 230  # 230.4
+    assert oracle_lib.dropout_threshold(1 - 0.5 / 256) == 1  # 0.5 rounds up
+    with pytest.raises(ValueError):
+        oracle_lib.dropout_threshold(0.999)  # keeps nothing
+    with pytest.raises(ValueError):
+        oracle_lib.dropout_threshold(-0.1)
+
+
+def test_dropout_zero_is_attention(oracle_lib):
+    rng = np.random.default_rng(3)
+    q, k, v = (rng.standard_normal((2, 2, 37, 16)) for _ in range(3))
+    for causal in (False, True):
+        o0, l0 = oracle_lib.attention(q, k, v, scale=0.3, causal=causal)
+        o1, l1 = oracle_lib.attention_dropout(q, k, v, 0.0, seed=5, scale=0.3, causal=causal)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+
+
+def test_dropout_weights_through_identity_values(oracle_lib):
+    """With V = I (Nk = d) each output row is the row's weights: the undropped
+    softmax probabilities times keep / q, not renormalised over the kept keys; lse is
+    the undropped one."""
+    rng = np.random.default_rng(4)
+    B, H, N = 1, 2, 48
+    q, k = rng.standard_normal((B, H, N, N)), rng.standard_normal((B, H, N, N))
+    v = np.broadcast_to(np.eye(N), (B, H, N, N)).copy()
+    for causal in (False, True):
+        P, l0 = oracle_lib.attention(q, k, v, scale=0.2, causal=causal)  # V = I: out is P
+        o, l1 = oracle_lib.attention_dropout(q, k, v, 0.25, seed=77, offset=3, scale=0.2, causal=causal)
+        keep = oracle_lib.dropout_keep(B, H, N, N, 0.25, 77, 3)
+        assert np.array_equal(l0, l1)
+        np.testing.assert_allclose(o, P * keep * (256 / 192), rtol=1e-12, atol=1e-15)
+
+
+def test_dropout_is_unbiased_over_seeds(oracle_lib):
+    """The mean over many seeds approaches the undropped output (E[keep / q] = 1)."""
+    rng = np.random.default_rng(5)
+    q, k, v = (rng.standard_normal((1, 1, 8, 8)) for _ in range(3))
+    o0, _ = oracle_lib.attention(q, k, v, scale=0.5)
+    acc = np.zeros_like(o0)
+    n = 3000
+    for s in range(n):
+        acc += oracle_lib.attention_dropout(q, k, v, 0.5, seed=s, scale=0.5)[0]
+    assert np.max(np.abs(acc / n - o0)) < 0.08
+
+
+def test_dropout_keep_fraction(oracle_lib):
+    keep = oracle_lib.dropout_keep(2, 4, 256, 256, 0.2, seed=2024)
+    t = oracle_lib.dropout_threshold(0.2)
+    frac, n = keep.mean(), keep.size
+    assert abs(frac - t / 256) < 5 * math.sqrt((t / 256) * (1 - t / 256) / n)
+    # different seeds, offsets and heads give different streams
+    assert not np.array_equal(keep, oracle_lib.dropout_keep(2, 4, 256, 256, 0.2, seed=2025))
+    assert not np.array_equal(keep, oracle_lib.dropout_keep(2, 4, 256, 256, 0.2, seed=2024, offset=1))
+    assert not np.array_equal(keep[0, 0], keep[0, 1])
