@@ -20,7 +20,7 @@ MUTANTS = [
     ("key_index_transposed", "for (int64_t t = 0; t < d; ++t) dot += qi[t] * kb[j * d + t];",
      "for (int64_t t = 0; t < d; ++t) dot += qi[t] * kb[t * Nk + j];"),
     ("head_index_swapped", "const double *kb = k + (b * H + h) * Nk * d;", "const double *kb = k + (h * H + b) * Nk * d;"),
-    ("lse_without_log", "*lse = m + log(l);", "*lse = m + l;"),
+    ("lse_without_log", "o[t] /= l;\n    *lse = m + log(l);", "o[t] /= l;\n    *lse = m + l;"),
     ("no_normalisation", "for (int64_t t = 0; t < d; ++t) o[t] /= l;", ";"),
     ("merge_without_rescale", "double fa = (mA == -INFINITY) ? 0.0 : exp(mA - mx);",
      "double fa = (mA == -INFINITY) ? 0.0 : 1.0;"),
