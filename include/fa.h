@@ -53,7 +53,8 @@ typedef enum {
     FA_ERR_LAUNCH = -5,      /* the CUDA launch (or tensor-map encoding) failed */
     FA_ERR_TIMEOUT = -6,     /* a device-side wait gave up (device status word) */
     FA_ERR_WORKSPACE = -7,   /* workspace missing or smaller than the problem needs */
-    FA_ERR_SEQLENS = -8      /* packed batch: cu_seqlens inconsistent (device status word) */
+    FA_ERR_SEQLENS = -8,     /* packed batch: cu_seqlens inconsistent (device status word) */
+    FA_ERR_ARG = -9          /* an argument is outside its range (dropout probability) */
 } fa_status;
 
 /* bf16 Q/K/V/out, fp32 accumulation. d in {64, 128}. */
@@ -144,6 +145,29 @@ int fa_fwd_masked(const void *q, const void *k, const void *v, const float *mask
 int fa_fwd_masked_fp16(const void *q, const void *k, const void *v, const float *mask, void *out, float *lse, int B,
                        int H, int Hkv, int N, int d, float scale, int causal, void *workspace,
                        unsigned long long workspace_bytes, void *stream);
+
+/* ---- dropout --------------------------------------------------------------
+ * The forward of fa_fwd_gqa / fa_fwd_gqa_fp16 (no mask) with dropout on the
+ * attention probabilities ("IO-aware exact attention", section "Why
+ * implementations form a family", names dropout as a variant of the
+ * calculation): out_i = sum_j P_ij keep_ij / q v_j, with P the softmax of the
+ * undropped scores; lse is unchanged. keep_ij is 1 with probability
+ * q = t / 256, t = floor((1 - p_drop) * 256 + 0.5), as follows:
+ *   keep_ij = [byte (j mod 32) of Philox4x64-10(counter = {i, j / 32, b*H + h,
+ *              offset}, key = {seed, 0}) < t],
+ * bytes numbered from the least significant byte of output word 0 upward.
+ * Philox4x64-10 is the counter-based generator of Salmon, Moraes, Dror and
+ * Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC 2011). The same
+ * (seed, offset) gives the same keep pattern on every call; callers advance
+ * `offset` (or change `seed`) between steps. p_drop = 0 gives fa_fwd_gqa's
+ * results bit for bit. Errors as for fa_fwd_gqa; FA_ERR_ARG if t < 1 (p_drop
+ * keeps nothing) or p_drop < 0 or NaN. */
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Hkv, int N,
+                   int d, float scale, int causal, float p_drop, unsigned long long seed, unsigned long long offset,
+                   void *stream);
+int fa_fwd_dropout_fp16(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Hkv,
+                        int N, int d, float scale, int causal, float p_drop, unsigned long long seed,
+                        unsigned long long offset, void *stream);
 
 /* ---- split-KV forward for decoding ------------------------------------------
  * Same operation for Nq query rows (1 <= Nq <= 16) against Nk >= 1 keys:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libfa.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_fp16.cu", "fa_fwd_mask_bf16.cu", "fa_fwd_mask_fp16.cu",
-           "fa_mask_pack.cu", "fa_fwd_fp32.cu", "fa_splitkv.cu", "fa_splitkv_noalloc.cu", "fa_bwd.cu",
+           "fa_mask_pack.cu", "fa_fwd_drop_bf16.cu", "fa_fwd_drop_fp16.cu", "fa_fwd_fp32.cu", "fa_splitkv.cu", "fa_splitkv_noalloc.cu", "fa_bwd.cu",
            "fa_fwd_varlen_bf16.cu", "fa_fwd_varlen_fp16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

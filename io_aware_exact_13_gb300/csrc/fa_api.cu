@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -166,6 +167,51 @@ int fwd_common(Type ty, const void *q, const void *k, const void *v, const float
         case Type::FP32: rc = fa::launch_fwd_fp32(a); break;
     }
     return rc;
+}
+
+// Keep threshold of drop probability p: (1 - p) rounded to a multiple of 1/256 (halves up), as
+// the count of byte values that keep; 0 when nothing would be kept (or p < 0, or p is NaN).
+int dropout_threshold(float p_drop) {
+    const double x = std::floor((1.0 - static_cast<double>(p_drop)) * 256.0 + 0.5);
+    if (!(x >= 1.0 && x <= 256.0)) return 0;
+    return static_cast<int>(x);
+}
+
+int dropout_common(Type ty, const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Hkv,
+                   int N, int d, float scale, int causal, float p_drop, unsigned long long seed,
+                   unsigned long long offset, void *stream) {
+    int rc = check_args(ty, q, k, v, nullptr, out, lse, B, H, N, d);
+    if (rc != FA_OK) return rc;
+    if (Hkv < 1 || H % Hkv != 0) return FA_ERR_SHAPE;
+    const int t = dropout_threshold(p_drop);
+    if (!(p_drop >= 0.0f) || t == 0) return FA_ERR_ARG;
+    log_call("forward with dropout %s d=%d causal=%d B=%d H=%d Hkv=%d N=%d p=%g (keep %d/256) seed=%llu offset=%llu",
+             ty == Type::BF16 ? "bf16" : "fp16", d, causal ? 1 : 0, B, H, Hkv, N, static_cast<double>(p_drop), t, seed,
+             offset);
+    DeviceInfo *di = device_info();
+    if (!di || !encoder()) return FA_ERR_LAUNCH;
+    fa::LaunchArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.mask = nullptr;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.Hkv = Hkv;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status = di->status;
+    a.num_sms = di->num_sms;
+    a.timeout_ns = kDefaultTimeoutNs;
+    a.drop_threshold = t;
+    a.drop_seed = seed;
+    a.drop_offset = offset;
+    return ty == Type::BF16 ? fa::launch_fwd_drop_bf16(a) : fa::launch_fwd_drop_fp16(a);
 }
 
 // bytes of the masked forward's workspace: the packed mask, then the packing pass's verdict word
@@ -498,6 +544,20 @@ int fa_fwd_masked_fp16(const void *q, const void *k, const void *v, const float 
                          workspace_bytes, stream);
 }
 
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Hkv, int N,
+                   int d, float scale, int causal, float p_drop, unsigned long long seed, unsigned long long offset,
+                   void *stream) {
+    return dropout_common(Type::BF16, q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, p_drop, seed, offset,
+                          stream);
+}
+
+int fa_fwd_dropout_fp16(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int Hkv,
+                        int N, int d, float scale, int causal, float p_drop, unsigned long long seed,
+                        unsigned long long offset, void *stream) {
+    return dropout_common(Type::FP16, q, k, v, out, lse, B, H, Hkv, N, d, scale, causal, p_drop, seed, offset,
+                          stream);
+}
+
 int fa_fwd_fp32(const void *q, const void *k, const void *v, const float *mask_or_null, void *out, float *lse,
                 int B, int H, int N, int d, float scale, int causal, void *stream) {
     return fwd_common(Type::FP32, q, k, v, mask_or_null, out, lse, B, H, N, d, scale, causal, stream);
@@ -633,6 +693,7 @@ const char *fa_status_string(int status) {
         case FA_ERR_TIMEOUT: return "a device-side pipeline wait timed out";
         case FA_ERR_WORKSPACE: return "workspace missing or smaller than the problem needs";
         case FA_ERR_SEQLENS: return "cu_seqlens inconsistent with total or max_seqlen (device status)";
+        case FA_ERR_ARG: return "an argument is outside its range (dropout: the drop probability keeps nothing)";
         default: return "unknown status";
     }
 }

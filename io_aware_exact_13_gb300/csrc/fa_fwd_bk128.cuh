@@ -136,15 +136,44 @@ __device__ __forceinline__ float row_max128(const float (&x)[128]) {
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
+// Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC 2011): ten rounds on a 256-bit counter; each multiplies counter words 0 and 2
+// by the two multipliers and mixes the halves of the products with words 1 and 3 and the round
+// key, which the two Weyl constants bump between rounds. The 256-bit result is returned as
+// eight 32-bit words, least significant first.
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t c1, uint64_t c2, uint64_t c3, uint64_t k0,
+                                              uint64_t k1, uint32_t (&w)[8]) {
+    constexpr uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    constexpr uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t lo0 = M0 * c0, hi0 = __umul64hi(M0, c0);
+        const uint64_t lo1 = M1 * c2, hi1 = __umul64hi(M1, c2);
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+    w[0] = (uint32_t)c0, w[1] = (uint32_t)(c0 >> 32), w[2] = (uint32_t)c1, w[3] = (uint32_t)(c1 >> 32);
+    w[4] = (uint32_t)c2, w[5] = (uint32_t)(c2 >> 32), w[6] = (uint32_t)c3, w[7] = (uint32_t)(c3 >> 32);
+}
+
 // MASK: an additive [B][N][N] mask whose entries are all 0 or -inf, in its packed form
 // (p.mask_bits, one bit per entry, set = -inf; see fa_mask_pack.cu). Thread r reads the 16
 // bytes of its row and key block from global memory (L2: the packed mask of a batch index is
 // shared by its heads), one block ahead of its use.
-template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false>
+// DROP: dropout ("IO-aware exact attention", section "Why implementations form a family",
+// names the variant). The softmax keeps the row maximum and sum of the undropped scores (lse
+// is unchanged); P is stored with dropped keys set to 0, and the epilogue multiplies O by
+// 1 / q. The keep bytes of a 32-key group come from one Philox block (see FwdParams).
+template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false, bool DROP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bk128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     static_assert(!(VARLEN && MASK), "no mask in a packed batch");
+    static_assert(!(DROP && (VARLEN || MASK)), "dropout with dense unmasked inputs only");
     using C = Cfg128<T, D>;
     constexpr int RK = C::RK, RV = C::RV;
     if constexpr (MASK) {  // the mask had other values: the 64-key kernel applies it as given
@@ -502,13 +531,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pv[32];
+                    if constexpr (DROP) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int i = 64 * hh + 2 * c;
-                        const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
-                        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-                        ls[c & 3] = fadd2(ls[c & 3], e);
-                        pv[c] = pack2<T>(e.x, e.y);
+                        for (int gq = 0; gq < 2; ++gq) {  // 32-key groups: one Philox block each
+                            uint32_t kw[8];
+                            philox4x64_10((uint64_t)row, (uint64_t)(4 * j + 2 * hh + gq), (uint64_t)bh, p.drop_offset,
+                                          p.drop_seed, 0ull, kw);
+#pragma unroll
+                            for (int c2 = 0; c2 < 16; ++c2) {
+                                const int c = 16 * gq + c2;
+                                const int i = 64 * hh + 2 * c;
+                                const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
+                                const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                                ls[c & 3] = fadd2(ls[c & 3], e);  // the row sum is of the undropped scores
+                                const uint32_t w = kw[c2 / 2];    // keys 2 c2, 2 c2 + 1 of the group: bytes of w
+                                const uint32_t b0 = (w >> (16 * (c2 & 1))) & 0xFFu, b1 = (w >> (16 * (c2 & 1) + 8)) & 0xFFu;
+                                pv[c] = pack2<T>(b0 < (uint32_t)p.drop_threshold ? e.x : 0.0f,
+                                                 b1 < (uint32_t)p.drop_threshold ? e.y : 0.0f);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int i = 64 * hh + 2 * c;
+                            const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
+                            const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                            ls[c & 3] = fadd2(ls[c & 3], e);
+                            pv[c] = pack2<T>(e.x, e.y);
+                        }
                     }
                     // P V(g-1), the tile's previous product, read P_t and accumulated into O_t:
                     // wait for its commit before overwriting P_t (and before rescaling O_t below).
@@ -542,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_warp(sy.pv_done(t, (g - 1) & 1u), ((g - 1) >> 1) & 1u, abort_flag, p);
             if (!ok) break;
             tc_fence_after();
-            const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+            float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+            if constexpr (DROP) inv *= p.drop_scale;  // kept probabilities are scaled by 1 / q
             const size_t orow_idx = VARLEN ? ((size_t)(itm.tok0 + row) * p.H + (size_t)(bh % p.H))
                                            : ((size_t)bh * p.N + (size_t)row);
             T *orow = reinterpret_cast<T *>(p.out) + orow_idx * D;

@@ -1,0 +1,10 @@
+// bf16 instantiations of the forward with dropout (the 128-key-block kernel).
+#include "fa_launch.cuh"
+
+namespace fa {
+int launch_fwd_drop_bf16(const LaunchArgs &a) {
+    if (a.d == 128) return launch_drop_fwd_d<__nv_bfloat16, 128>(a);
+    if (a.d == 64) return launch_drop_fwd_d<__nv_bfloat16, 64>(a);
+    return -4;
+}
+}  // namespace fa

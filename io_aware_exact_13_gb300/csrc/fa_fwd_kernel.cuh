@@ -140,6 +140,12 @@ struct FwdParams {
     const uint4 *mask_bits;
     int mask_bits_blk;
     const int *mask_kind;
+    // Dropout (128-key kernel): key j of query row i of head bh is kept when byte j mod 32 of
+    // Philox4x64-10(counter {i, j / 32, bh, drop_offset}, key {drop_seed, 0}) is below drop_threshold
+    // (1..256); kept probabilities are scaled by drop_scale = 256 / drop_threshold.
+    uint64_t drop_seed, drop_offset;
+    int drop_threshold;
+    float drop_scale;
 };
 
 // Static schedule: CTA c takes item w*G + c in even waves w and w*G + (G-1-c)

@@ -31,6 +31,9 @@ struct LaunchArgs {
     // nullptr: the fp32 mask is applied as given
     const void *mask_bits = nullptr;
     const int *mask_kind = nullptr;
+    // dropout: keep threshold 1..256 (0 = no dropout), Philox key and counter offset
+    int drop_threshold = 0;
+    uint64_t drop_seed = 0, drop_offset = 0;
 };
 
 // Defined in fa_mask_pack.cu: bytes of the packed form of a [rows][nk] mask, and the packing pass
@@ -108,6 +111,9 @@ int launch_variant(const LaunchArgs &a) {
     p.mask_bits = nullptr;
     p.mask_bits_blk = 0;
     p.mask_kind = MASK ? a.mask_kind : nullptr;
+    p.drop_seed = p.drop_offset = 0;
+    p.drop_threshold = 256;
+    p.drop_scale = 1.0f;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     if (MASK && a.mask_kind != nullptr)  // behind the 128-key kernel on the packed mask (see launch_mask_fwd_d)
         return launch_dependent(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, a.stream, tq, tk, tv, tm, p) ==
@@ -119,13 +125,14 @@ int launch_variant(const LaunchArgs &a) {
 }
 
 // The 128-key-block kernel: dense [B][H][N][d] tensors, or a packed batch; MASK: a shared
-// [B][N][N] mask in its packed one-bit form.
-template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false>
+// [B][N][N] mask in its packed one-bit form; DROP: dropout (dense, no mask).
+template <typename T, int D, bool CAUSAL, bool VARLEN, bool MASK = false, bool DROP = false>
 int launch_bk128(const LaunchArgs &a) {
     static_assert(!(VARLEN && MASK), "no mask in a packed batch");
     using C = Cfg128<T, D>;
-    auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN, MASK>;
+    auto kern = fa_fwd_bk128_kernel<T, D, CAUSAL, VARLEN, MASK, DROP>;
     if (MASK && (a.mask_bits == nullptr || a.mask_kind == nullptr)) return -5;
+    if (DROP && (a.drop_threshold < 1 || a.drop_threshold > 256)) return -5;
     // The register split between warpgroups assumes 128 registers per thread at
     // launch (512 x 128 = 256 x 184 + 256 x 72). Refuse to launch otherwise.
     cudaFuncAttributes attr;
@@ -171,6 +178,10 @@ int launch_bk128(const LaunchArgs &a) {
     p.mask_bits = MASK ? static_cast<const uint4 *>(a.mask_bits) : nullptr;
     p.mask_bits_blk = MASK ? (a.N + kBK128 - 1) / kBK128 : 0;
     p.mask_kind = MASK ? a.mask_kind : nullptr;
+    p.drop_seed = DROP ? a.drop_seed : 0;
+    p.drop_offset = DROP ? a.drop_offset : 0;
+    p.drop_threshold = DROP ? a.drop_threshold : 256;
+    p.drop_scale = DROP ? static_cast<float>(256.0 / a.drop_threshold) : 1.0f;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
     kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
@@ -203,5 +214,13 @@ int launch_mask_fwd_d(const LaunchArgs &a) {
 
 int launch_fwd_mask_bf16(const LaunchArgs &a);  // fa_fwd_mask_bf16.cu
 int launch_fwd_mask_fp16(const LaunchArgs &a);  // fa_fwd_mask_fp16.cu
+int launch_fwd_drop_bf16(const LaunchArgs &a);  // fa_fwd_drop_bf16.cu
+int launch_fwd_drop_fp16(const LaunchArgs &a);  // fa_fwd_drop_fp16.cu
+
+// A forward with dropout (dense, no mask).
+template <typename T, int D>
+int launch_drop_fwd_d(const LaunchArgs &a) {
+    return a.causal ? launch_bk128<T, D, true, false, false, true>(a) : launch_bk128<T, D, false, false, false, true>(a);
+}
 
 }  // namespace fa

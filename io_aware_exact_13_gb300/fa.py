@@ -7,6 +7,7 @@ has not been built, and every call raises if the library returns an error.
 
 Names follow the C ABI: ``fa_fwd`` (bf16), ``fa_fwd_fp16``, ``fa_fwd_fp32``,
 ``fa_fwd_masked`` / ``fa_fwd_masked_fp16`` (a shared mask packed in a workspace),
+``fa_fwd_dropout`` / ``fa_fwd_dropout_fp16`` (dropout on the probabilities),
 ``fa_fwd_splitkv`` / ``fa_fwd_splitkv_fp16`` (decoding), ``fa_bwd`` /
 ``fa_bwd_fp16`` (backward by recomputation), ``fa_fwd_varlen`` /
 ``fa_fwd_varlen_fp16`` (packed variable-length batches), their sizing helpers,
@@ -38,6 +39,7 @@ FA_ERR_LAUNCH = -5
 FA_ERR_TIMEOUT = -6
 FA_ERR_WORKSPACE = -7
 FA_ERR_SEQLENS = -8
+FA_ERR_ARG = -9
 
 # Every symbol the header declares, with its ctypes signature.
 _vp = ctypes.c_void_p
@@ -54,6 +56,11 @@ SIGNATURES = {
     "fa_fwd_bias_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_gqa": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp]),
     "fa_fwd_masked_workspace_bytes": (ctypes.c_longlong, [ctypes.c_int] * 2),
+    "fa_fwd_dropout": (ctypes.c_int, [_vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, ctypes.c_float,
+                                                                       ctypes.c_ulonglong, ctypes.c_ulonglong, _vp]),
+    "fa_fwd_dropout_fp16": (ctypes.c_int, [_vp] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                                            ctypes.c_float, ctypes.c_ulonglong,
+                                                                            ctypes.c_ulonglong, _vp]),
     "fa_fwd_masked": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp,
                                                                         ctypes.c_ulonglong, _vp]),
     "fa_fwd_masked_fp16": (ctypes.c_int, [_vp] * 6 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int, _vp,
@@ -209,6 +216,46 @@ def fa_fwd_masked_fp16(q, k, v, mask, out, lse, scale, causal, workspace, stream
 
 
 _MASKED = {torch.bfloat16: fa_fwd_masked, torch.float16: fa_fwd_masked_fp16}
+
+
+# ---------------------------------------------------------------- dropout
+def _fwd_dropout(fn_name, dtype, q, k, v, out, lse, scale, causal, p_drop, seed, offset, stream):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape or out.shape != q.shape or H % Hkv:
+        raise ValueError("q, out: [B, H, N, d]; k, v: [B, Hkv, N, d] with Hkv dividing H")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA float32 [B, H, N] tensor")
+    rc = getattr(lib, fn_name)(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d, float(scale),
+                               int(bool(causal)), float(p_drop), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if rc != FA_OK:
+        raise FAError(rc, fn_name)
+
+
+def fa_fwd_dropout(q, k, v, out, lse, scale, causal, p_drop, seed, offset=0, stream=None):
+    """bf16 forward with dropout: keep decisions from Philox4x64-10 keyed by ``seed``, counter
+    {query row, key / 32, b*H + h, ``offset``}; k, v may hold fewer heads (grouped-query)."""
+    _fwd_dropout("fa_fwd_dropout", torch.bfloat16, q, k, v, out, lse, scale, causal, p_drop, seed, offset, stream)
+
+
+def fa_fwd_dropout_fp16(q, k, v, out, lse, scale, causal, p_drop, seed, offset=0, stream=None):
+    """fp16 forward with dropout (see ``fa_fwd_dropout``)."""
+    _fwd_dropout("fa_fwd_dropout_fp16", torch.float16, q, k, v, out, lse, scale, causal, p_drop, seed, offset, stream)
+
+
+def attention_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False, stream=None):
+    """Forward with dropout; allocates O and lse."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fn = {torch.bfloat16: fa_fwd_dropout, torch.float16: fa_fwd_dropout_fp16}[q.dtype]
+    fn(q, k, v, out, lse, scale, causal, p_drop, seed, offset, stream)
+    return out, lse
 
 
 # ---------------------------------------------------------------- forward from host memory

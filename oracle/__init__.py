@@ -227,7 +227,7 @@ def attention_bwd(q, k, v, dout, mask=None, scale=None, causal=False):
 def dropout_threshold(p_drop: float) -> int:
     """Keep threshold of drop probability p: the keep probability (1 - p) rounded to a
     multiple of 1/256 (halves up), as a count of the 256 byte values that keep."""
-    t = int(np.floor((1.0 - float(p_drop)) * 256.0 + 0.5))
+    t = int(np.floor((1.0 - float(p_drop)) * 256.0 + 0.5)) if float(p_drop) >= 0.0 else 0
     if not 1 <= t <= 256:
         raise ValueError(f"drop probability {p_drop} keeps nothing (or is negative)")
     return t

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 
 def test_status_strings(fa):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         s = fa.fa_status_string(code)
         assert s and s != "unknown status"
     assert fa.fa_status_string(12345) == "unknown status"
@@ -256,3 +256,22 @@ def test_masked_workspace_size(fa):
     assert fa.fa_fwd_masked_workspace_bytes(3, 129) == 3 * 129 * 2 * 16 + 256
     with pytest.raises(fa.FAError):
         fa.fa_fwd_masked_workspace_bytes(0, 16)
+
+
+@pytest.mark.parametrize("name", ["fa_fwd_dropout", "fa_fwd_dropout_fp16"])
+def test_dropout_host_validation(fa, name):
+    f = getattr(fa.lib, name)
+
+    def call(q=0x10000, H=4, Hkv=2, N=300, d=128, p_drop=0.1):
+        return f(ctypes.c_void_p(q) if q else None, ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000),
+                 ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000), 2, H, Hkv, N, d, ctypes.c_float(0.1), 0,
+                 ctypes.c_float(p_drop), 7, 0, None)
+
+    assert call(q=0) == fa.FA_ERR_NULL
+    assert call(q=0x10008) == fa.FA_ERR_ALIGN
+    assert call(N=0) == fa.FA_ERR_SHAPE
+    assert call(Hkv=3) == fa.FA_ERR_SHAPE
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert call(p_drop=0.999) == fa.FA_ERR_ARG       # keeps nothing
+    assert call(p_drop=-0.001) == fa.FA_ERR_ARG
+    assert call(p_drop=float("nan")) == fa.FA_ERR_ARG

@@ -467,7 +467,7 @@ def test_dropout_threshold_rounding(oracle_lib):
     with pytest.raises(ValueError):
         oracle_lib.dropout_threshold(0.999)  # keeps nothing
     with pytest.raises(ValueError):
-        oracle_lib.dropout_threshold(-0.1)
+        oracle_lib.dropout_threshold(-0.001)
 
 
 def test_dropout_zero_is_attention(oracle_lib):
