@@ -273,7 +273,7 @@ def run_ours(args, w):
 
     entry = {"bf16": fa.fa_fwd, "fp16": fa.fa_fwd_fp16, "fp32": fa.fa_fwd_fp32}[w.dtype]
     q, k, v, mask = make_workload(w)
-    if mask is not None and w.dtype in ("bf16", "fp16"):
+    if mask is not None and w.dtype in ("bf16", "fp16") and not args.fp32_mask:
         # the masked entry point with its workspace: the mask is packed to one bit per entry in every call
         masked_fn = fa.fa_fwd_masked if w.dtype == "bf16" else fa.fa_fwd_masked_fp16
         mask_ws = torch.empty(fa.fa_fwd_masked_workspace_bytes(w.B, w.N), dtype=torch.uint8, device=dev)
@@ -399,9 +399,11 @@ def run_ours(args, w):
         peak, peak_src = 2 * 128 * fa.fa_num_sms() * 2.07e9 / 1e12, "fp32 FFMA rate at 2070 MHz (unit counts)"
     roofline = {"bound": "alu" if w.dtype == "fp32" else "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None if w.dtype == "fp32" else load_traffic(w.name, "fa_fwd_bk128_kernel"),
+                "traffic": (None if w.dtype == "fp32" else
+                            load_traffic(w.name, "fa_fwd_kernel" if args.fp32_mask else "fa_fwd_bk128_kernel")),
                 "peak_source": peak_src,
                 "kernel": ("fa_fwd_fp32_kernel" if w.dtype == "fp32" else
+                           "fa_fwd_kernel (64-key blocks, fp32 mask)" if (w.has_mask and args.fp32_mask) else
                            "fa_fwd_bk128_kernel (mask packed to one bit per entry; the timed call includes the "
                            "packing pass)" if w.has_mask else "fa_fwd_bk128_kernel"),
                 "launch_ms_mean": 1e3 * mean_launch_s,
@@ -427,8 +429,14 @@ def run_ours(args, w):
         "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": (f"fa_fwd_host, {E2E_CHUNKS} head chunks, copies pipelined with the forward"
-                         if host_entry is not None else "copy in, fa_fwd, copy out")},
-        "gpu_launches": args.steps * len(rep_ms),
+                         if host_entry is not None else
+                         "copy in (mask included), fa_fwd_masked with its workspace, copy out"
+                         if (w.has_mask and w.dtype != "fp32" and not args.fp32_mask) else
+                         "copy in, fa_fwd, copy out")},
+        # kernels per call: the forward; with a mask also the packing pass and the fp32-mask kernel (which
+        # returns at once for a 0/-inf mask)
+        "gpu_launches": args.steps * len(rep_ms) * (3 if (w.has_mask and w.dtype != "fp32" and not args.fp32_mask)
+                                                    else 1),
         "roofline": roofline,
         "clocks": clocks,
     }
@@ -738,6 +746,8 @@ def main():
     ap.add_argument("--cpu-sample-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp32-mask", action="store_true",
+                    help="masked workload through fa_fwd / fa_fwd_fp16 without a workspace (the fp32-mask kernel)")
     ap.add_argument("--timed-s", type=float, default=2.0,
                     help="repeat the K-step timed region until about this many seconds are covered")
     ap.add_argument("--max-repeats", type=int, default=200)

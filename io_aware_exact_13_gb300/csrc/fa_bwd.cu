@@ -309,11 +309,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 mma_ts(tmem + 256, tmem + 0 + pcol, do_mn + off, C::ID_ACC, acc, issue);
                 mma_ts(tmem + 256 + D, tmem + 128 + pcol, q_mn + off, C::ID_ACC, acc, issue);
             }
-            // dQ_i = dS K_j, contracted over the 128 keys, 64 head columns at a time
+            // dQ_i = dS K_j, contracted over the 128 keys, 64 head columns at a time; the halves'
+            // accumulation chains are interleaved (a chain completes about one product per 77 cycles)
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h)
+            for (int k = 0; k < C::KSTEPS_R; ++k)
 #pragma unroll
-                for (int k = 0; k < C::KSTEPS_R; ++k) {
+                for (int h = 0; h < D / 64; ++h) {
                     const uint64_t off = (uint64_t)((k * 2048) >> 4);
                     mma_ss(tmem + (h == 0 ? 32 : 160), ds_mn + off, k_mn + (uint64_t)((h * C::CHUNK) >> 4) + off,
                            C::ID_DQ, k > 0 ? 1u : 0u, issue);
