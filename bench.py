@@ -65,16 +65,24 @@ def workload_bytes(w) -> int:
     return n + (4 * w.B * w.N * w.N if w.has_mask else 0)
 
 
-def needs_flush(w) -> bool:
-    """Inputs that fit in L2 (with room to spare) are timed with an L2 flush between steps."""
+def fits_in_l2(w) -> bool:
+    """Inputs and outputs that L2 could hold (with room to spare): timed on rotating copies (l2_copies)."""
     return workload_bytes(w) < 2 * L2_BYTES
+
+
+def l2_copies(w) -> int:
+    """Copies of a workload that fits in L2, used in turn step by step: a copy comes back only after
+    more than twice the L2 has been touched by the others."""
+    return int(math.ceil(2 * L2_BYTES / workload_bytes(w))) + 1
 
 
 def bench_config(w, world: int, split: bool = False) -> dict:
     """The ``config`` object of both arms' JSON lines (the same workload, the same keys)."""
     mb = workload_bytes(w) / 1e6
-    l2 = (f"inputs and outputs ({mb:.0f} MB) exceed the 126 MB L2; no flush between steps" if not needs_flush(w)
-          else f"inputs and outputs ({mb:.1f} MB) fit in L2; a 256 MB buffer is written between timed steps")
+    l2 = (f"inputs and outputs ({mb:.0f} MB) exceed the 126 MB L2; no flush between steps" if not fits_in_l2(w)
+          else f"inputs and outputs ({mb:.2f} MB) fit in L2: each step uses the next of {l2_copies(w)} copies "
+               f"({l2_copies(w) * mb:.0f} MB in all, so none is in L2 when it comes back), and the timed steps "
+               f"are replayed from CUDA graphs")
     par = (f"heads split over {world} ranks (one problem, no collective)" if split
            else f"replicas x{world} (independent problems, no collective)")
     return dict(w.describe(), l2=l2, parallelism=par)
@@ -305,8 +313,33 @@ def run_ours(args, w):
     # ---------------------------------------------------------------- device-resident timing
     # The K-step region is timed `repeats` times (each bracketed by a barrier and a synchronize) so
     # that the clock sampler sees the kernel for about a second; the median repeat is reported.
-    flush = needs_flush(w)
-    scratch = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+    # A workload that fits in L2 runs each step on the next of several copies of its tensors (so every
+    # step starts from DRAM) and replays the K steps from CUDA graphs, one per group of K copies: host
+    # launch overhead and an L2 flush between steps would otherwise be what the events measure.
+    rotate = fits_in_l2(w)
+    graphs = []
+    if rotate:
+        n_copies = l2_copies(w)
+        copies = [(qd.clone(), kd.clone(), vd.clone(), None if md is None else md.clone(), torch.empty_like(od),
+                   torch.empty_like(lsed)) for _ in range(n_copies)]
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        for g0 in range(0, n_copies, args.steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                for i in range(args.steps):  # every copy once before the capture (warm-up)
+                    c = copies[(g0 + i) % n_copies]
+                    entry(c[0], c[1], c[2], c[3], c[4], c[5], w.scale, w.causal, cap)
+            cap.synchronize()
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(args.steps):
+                    c = copies[(g0 + i) % n_copies]
+                    entry(c[0], c[1], c[2], c[3], c[4], c[5], w.scale, w.causal, cap)
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+        for g in graphs:  # warm replays
+            g.replay()
+        torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index) if rank == 0 else None
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -318,27 +351,33 @@ def run_ours(args, w):
         sampler.start()
         time.sleep(0.3)
     launch_ms, rep_ms = [], []
-    for _ in range(repeats):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    for rep in range(repeats):
         barrier(world, dev)
         torch.cuda.synchronize(dev)
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            if flush:
-                scratch.fill_(i & 255)
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
+        if rotate:
+            g = graphs[rep % len(graphs)]
+            t_start.record(stream)
+            g.replay()
+            t_end.record(stream)
+            torch.cuda.synchronize(dev)
+            region = t_start.elapsed_time(t_end)
+            launch_ms += [region / args.steps] * args.steps
+        else:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            t_start.record(stream)
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+            t_end.record(stream)
+            torch.cuda.synchronize(dev)
+            launch_ms += [a.elapsed_time(b) for a, b in ev]
+            region = t_start.elapsed_time(t_end)
         barrier(world, dev)
-        ms = [a.elapsed_time(b) for a, b in ev]
-        launch_ms += ms
-        # with a flush between steps the region's time is the sum of the launches
-        rep_ms.append(max_over_ranks(world, sum(ms) if flush else t_start.elapsed_time(t_end), dev))
+        rep_ms.append(max_over_ranks(world, region, dev))
     clocks = sampler.stop() if sampler else None
     total_ms = statistics.median(rep_ms)
     status = fa.fa_get_device_status(stream)
@@ -750,7 +789,7 @@ def main():
                     help="masked workload through fa_fwd / fa_fwd_fp16 without a workspace (the fp32-mask kernel)")
     ap.add_argument("--timed-s", type=float, default=2.0,
                     help="repeat the K-step timed region until about this many seconds are covered")
-    ap.add_argument("--max-repeats", type=int, default=200)
+    ap.add_argument("--max-repeats", type=int, default=5000)
     ap.add_argument("--partition", choices=["replicas", "heads"], default="replicas",
                     help="N>1: every rank runs the whole workload (replicas, weak scaling) or one share of its "
                          "heads (heads, strong scaling)")
