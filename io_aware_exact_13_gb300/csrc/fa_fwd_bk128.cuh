@@ -494,13 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(sy.s_free());  // the S buffer may now take the next product
                 if constexpr (MASK) {
-                    // bit e of word c is key 4 e + c of the block; the next block's bits are loaded now
+                    // bit e of word c is key 4 e + c of the block; the next block's bits are loaded now. A block
+                    // in which no row of the warp has a masked key is skipped (padding and block-structured masks).
                     const uint4 nb = (j + 1 < nt) ? __ldg(bits_row + j + 1) : make_uint4(0u, 0u, 0u, 0u);
-                    const uint32_t w[4] = {bits.x, bits.y, bits.z, bits.w};
+                    if (__any_sync(0xffffffffu, (bits.x | bits.y | bits.z | bits.w) != 0u)) {
+                        const uint32_t w[4] = {bits.x, bits.y, bits.z, bits.w};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) x[4 * e + c] = ((w[c] >> e) & 1u) ? -INFINITY : x[4 * e + c];
+                            for (int e = 0; e < 32; ++e)
+                                x[4 * e + c] = ((w[c] >> e) & 1u) ? -INFINITY : x[4 * e + c];
+                        }
                     }
                     bits = nb;
                 }
