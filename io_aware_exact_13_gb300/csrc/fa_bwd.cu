@@ -492,8 +492,8 @@ struct BwdCfgH64 {
     static constexpr int SMEM_DS = SMEM_QD + STAGES * 2 * CHUNK;   // dS[2]: queries 0-63 | 64-127, 128 keys each
     static constexpr int SMEM_STATS = SMEM_DS + 4 * CHUNK;         // [half][buffer][-lse2 x64, -D x64]
     static constexpr int SMEM_BAR = SMEM_STATS + 2 * 2 * 128 * 4;
-    // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], dq_full, dq_free, stats[2], drain
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1;
+    // kv, qd_full[ST], qd_empty[ST], sp_full[2], p_full[2], dq_full, dq_free, stats[2], drain, acc_done[2]
+    static constexpr int NUM_BARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 2;
     static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;
     static constexpr uint32_t FMT = Elem<T>::fmt;
     static constexpr uint32_t ID_S = make_idesc_ab(FMT, 128, 64, 0, 0);   // S_h^T, dP_h^T: 128 keys x 64 queries
@@ -520,7 +520,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t bar_dq_full = smem_u32(bars + 5 + 2 * ST);                  // dQ of the block computed
     const uint32_t bar_dq_free = smem_u32(bars + 6 + 2 * ST);                  // dQ loaded by all (256 arrivals)
     auto bar_stats = [&](int h) { return smem_u32(bars + 7 + 2 * ST + h); };   // half h statistics (128 arrivals)
-    const uint32_t bar_drain = smem_u32(bars + 9 + 2 * ST);
+    const uint32_t bar_drain = smem_u32(bars + 9 + 2 * ST);                    // both issuing warps' products done
+    auto bar_acc_done = [&](int h) { return smem_u32(bars + 10 + 2 * ST + h); }; // dV, dK of half h done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -535,16 +536,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar_kv, 1);
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_qd_full(s), 1);
-            mbar_init(bar_qd_empty(s), 1);
+            mbar_init(bar_qd_empty(s), 2);  // the last S/dP product and the last dV/dK product of the stage
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(bar_sp_full(h), 1);
             mbar_init(bar_p_full(h), 128);
             mbar_init(bar_stats(h), 128);
+            mbar_init(bar_acc_done(h), 1);
         }
         mbar_init(bar_dq_full, 1);
         mbar_init(bar_dq_free, kGradThreads);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, 2);  // one commit per issuing warp
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -579,80 +581,104 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = issued - ST > 0 ? issued - ST : 0; it < issued; ++it)
                 bwd_wait(bar_qd_full(it % ST), (it / ST) & 1u, p);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ---------------------------------------------------------------- MMA issuers
+        // One warp issues about one product every 77 cycles, so the products are split over two
+        // warps: warp 1 issues every S/dP product, warp 2 the dV/dK products of each half and dQ of
+        // the block (the tensor core runs both streams). What one thread's order used to guarantee is
+        // explicit: a stage is released by a commit from each warp (qd_empty counts two), a half's
+        // packed P^T is overwritten by the next pass only after acc_done(h), and dQ(i) and dK(i, h)
+        // have read a half's dS rows by dq_full(i), which the warpgroup waits for before it stages dQ
+        // there or, a block later, writes dS there again.
         const uint32_t issue = lane == 0 ? 1u : 0u;
         const uint64_t k_km = smem_desc_sw128(smem_u32(smem + C::SMEM_K), 16, 1024);
         const uint64_t v_km = smem_desc_sw128(smem_u32(smem + C::SMEM_V), 16, 1024);
         const uint64_t k_mn = smem_desc_sw128(smem_u32(smem + C::SMEM_K), C::CHUNK, 1024);
-        // S_h^T = K_j Q_h^T, dP_h^T = V_j dO_h^T of block it (query rows 64h.. of the stage = +8 KB)
-        auto issue_s = [&](int it, int h) {
-            const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
-            const uint64_t q_km = smem_desc_sw128(q_s, 16, 1024);
-            const uint64_t do_km = smem_desc_sw128(q_s + C::CHUNK, 16, 1024);
-            const uint64_t hoff = (uint64_t)((h * 64 * 128) >> 4);
+        bool ok = bwd_wait_warp(bar_kv, 0, p);
+        if (warp == 1) {
+            // S_h^T = K_j Q_h^T, dP_h^T = V_j dO_h^T of block it (query rows 64h.. of the stage = +8 KB)
+            auto issue_s = [&](int it, int h) {
+                const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
+                const uint64_t q_km = smem_desc_sw128(q_s, 16, 1024);
+                const uint64_t do_km = smem_desc_sw128(q_s + C::CHUNK, 16, 1024);
+                const uint64_t hoff = (uint64_t)((h * 64 * 128) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t off = (uint64_t)((k * 32) >> 4);
-                mma_ss(tmem + 128 * h, k_km + off, q_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
-                mma_ss(tmem + 128 * h + 64, v_km + off, do_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t off = (uint64_t)((k * 32) >> 4);
+                    mma_ss(tmem + 128 * h, k_km + off, q_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
+                    mma_ss(tmem + 128 * h + 64, v_km + off, do_km + hoff + off, C::ID_S, k > 0 ? 1u : 0u, issue);
+                }
+                tc_commit(bar_sp_full(h), issue);
+            };
+            ok = ok && bwd_wait_warp(bar_qd_full(0), 0, p);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(0, 1);
+                tc_commit(bar_qd_empty(0), issue);  // this warp's last reader of stage 0
             }
-            tc_commit(bar_sp_full(h), issue);
-        };
-        // dV_j += P_h^T dO_h (A = packed P^T in TMEM), dK_j += dS_h^T Q_h (A = dS^T, K-major, from the
-        // block's dS buffer), contracted over the 64 rows of half h of block it
-        auto issue_acc = [&](int it, int h) {
-            const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
-            const uint64_t q_mn = smem_desc_sw128(q_s, C::CHUNK, 1024);
-            const uint64_t do_mn = smem_desc_sw128(q_s + C::CHUNK, C::CHUNK, 1024);
-            const uint64_t dst_km =
-                smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK + h * C::CHUNK), 16, 1024);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const bool next = it + 1 < n_it;
+                ok = bwd_wait_warp(bar_p_full(0), it & 1u, p);  // half A's S/dP columns were read
+                if (ok && next) {
+                    ok = bwd_wait_warp(bar_qd_full((it + 1) % ST), ((it + 1) / ST) & 1u, p);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(it + 1, 0);
+                    }
+                }
+                if (ok) ok = bwd_wait_warp(bar_p_full(1), it & 1u, p);
+                if (ok && next) {
+                    tc_fence_after();
+                    issue_s(it + 1, 1);
+                    tc_commit(bar_qd_empty((it + 1) % ST), issue);
+                }
+            }
+        } else {
+            // dV_j += P_h^T dO_h (A = packed P^T in TMEM), dK_j += dS_h^T Q_h (A = dS^T, K-major, from the
+            // block's dS buffer), contracted over the 64 rows of half h of block it
+            auto issue_acc = [&](int it, int h) {
+                const uint32_t q_s = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::CHUNK);
+                const uint64_t q_mn = smem_desc_sw128(q_s, C::CHUNK, 1024);
+                const uint64_t do_mn = smem_desc_sw128(q_s + C::CHUNK, C::CHUNK, 1024);
+                const uint64_t dst_km =
+                    smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK + h * C::CHUNK), 16, 1024);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint64_t off = (uint64_t)(((h * 64 + k * 16) * 128) >> 4);
-                const uint32_t acc = (it > 0 || h > 0 || k > 0) ? 1u : 0u;
-                mma_ts(tmem + 320, tmem + 256 + 32 * h + 8 * k, do_mn + off, C::ID_ACC, acc, issue);
-                mma_ss(tmem + 384, dst_km + (uint64_t)((k * 32) >> 4), q_mn + off, C::ID_ACC, acc, issue);
-            }
-        };
-        bool ok = bwd_wait_warp(bar_kv, 0, p) && bwd_wait_warp(bar_qd_full(0), 0, p);
-        if (ok) {
-            tc_fence_after();
-            issue_s(0, 0);
-            issue_s(0, 1);
-        }
-        for (int it = 0; ok && it < n_it; ++it) {
-            const bool next = it + 1 < n_it;
-            ok = bwd_wait_warp(bar_p_full(0), it & 1u, p);
-            if (!ok) break;
-            tc_fence_after();
-            issue_acc(it, 0);
-            if (next) {  // half A's S and dP columns were read by its pass: the next block may use them
-                ok = bwd_wait_warp(bar_qd_full((it + 1) % ST), ((it + 1) / ST) & 1u, p);
+                for (int k = 0; k < 4; ++k) {
+                    const uint64_t off = (uint64_t)(((h * 64 + k * 16) * 128) >> 4);
+                    const uint32_t acc = (it > 0 || h > 0 || k > 0) ? 1u : 0u;
+                    mma_ts(tmem + 320, tmem + 256 + 32 * h + 8 * k, do_mn + off, C::ID_ACC, acc, issue);
+                    mma_ss(tmem + 384, dst_km + (uint64_t)((k * 32) >> 4), q_mn + off, C::ID_ACC, acc, issue);
+                }
+                tc_commit(bar_acc_done(h), issue);
+            };
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int s = it % ST;
+                ok = bwd_wait_warp(bar_p_full(0), it & 1u, p) && bwd_wait_warp(bar_qd_full(s), (it / ST) & 1u, p);
                 if (!ok) break;
-                issue_s(it + 1, 0);
-            }
-            ok = bwd_wait_warp(bar_p_full(1), it & 1u, p);
-            if (!ok) break;
-            tc_fence_after();
-            issue_acc(it, 1);
-            tc_commit(bar_qd_empty(it % ST), issue);  // every reader of this Q, dO stage is issued
-            if (next) issue_s(it + 1, 1);
-            if (it > 0) ok = bwd_wait_warp(bar_dq_free, (it - 1) & 1u, p);  // dQ of the last block read out
-            if (!ok) break;
-            tc_fence_after();
-            // dQ_i = dS_i K_j, contracted over the 128 keys (dS buffer it & 1)
-            const uint64_t ds_mn =
-                smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK), C::CHUNK, 1024);
+                tc_fence_after();
+                issue_acc(it, 0);
+                ok = bwd_wait_warp(bar_p_full(1), it & 1u, p);
+                if (!ok) break;
+                tc_fence_after();
+                issue_acc(it, 1);
+                tc_commit(bar_qd_empty(s), issue);  // this warp's last reader of the stage
+                if (it > 0) ok = bwd_wait_warp(bar_dq_free, (it - 1) & 1u, p);  // dQ of the last block read out
+                if (!ok) break;
+                tc_fence_after();
+                // dQ_i = dS_i K_j, contracted over the 128 keys (dS buffer it & 1)
+                const uint64_t ds_mn =
+                    smem_desc_sw128(smem_u32(smem + C::SMEM_DS + (it & 1) * 2 * C::CHUNK), C::CHUNK, 1024);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                mma_ss(tmem + 448, ds_mn + off, k_mn + off, C::ID_DQ, k > 0 ? 1u : 0u, issue);
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                    mma_ss(tmem + 448, ds_mn + off, k_mn + off, C::ID_DQ, k > 0 ? 1u : 0u, issue);
+                }
+                tc_commit(bar_dq_full, issue);
             }
-            tc_commit(bar_dq_full, issue);
         }
         tc_commit(bar_drain, issue);
-        bwd_wait_warp(bar_drain, 0, p);
+        if (warp == 1) bwd_wait_warp(bar_drain, 0, p);  // both warps' products, before TMEM is freed
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- gradient warps
         const int g = (warp - 4) >> 2;  // half of the query block
@@ -697,6 +723,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the reduction of dQ(i - 2), staged in these rows, must have read them
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
+            // dV(i - 1, g) read this half's packed P^T before it is overwritten below
+            if (it > 0 && !bwd_wait_warp(bar_acc_done(g), (it - 1) & 1u, p)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t sv[32], dpv[32];

@@ -667,3 +667,163 @@ def simulate_bk128(N, causal, items, rk, rv, seed, rescale_prob=0.1, item_ring=0
             del agents[c]
             waiting[c] = None
     return True
+
+
+def simulate_bwd_split(n_it, stages, seed, acc_waits=True, qd_empty_count=2, acc_waits_dq_free=True,
+                       acc_waits_qd=True):
+    """The d = 64 backward with two issuing warps: warp 1 issues every S/dP product, warp 2 the
+    dV/dK products of each half and dQ of the block. Each warp's products run in order in their own
+    queue; the two queues interleave arbitrarily (they share the tensor core). Besides the barriers,
+    the model tracks what each buffer holds, so that these hazards fail here:
+      - P^T of half h overwritten by the next pass before dV(i, h) read it (acc_done(h) guards it);
+      - a Q/dO stage refilled before both warps' products read it (qd_empty takes two commits);
+      - the dQ columns overwritten before both warpgroups read dQ(i) out (dq_free);
+      - dS rows (the half's rows of buffer i & 1) overwritten, or used as dQ staging, before dK(i, h)
+        and dQ(i) read them;
+      - S/dP of a half overwritten before its pass read them.
+    Mutations that must be caught: acc_waits=False (no acc_done wait before the P^T store),
+    qd_empty_count=1, acc_waits_dq_free=False, acc_waits_qd=False is allowed (the p_full chain
+    orders the copies) but modelled to show the stage content is right either way."""
+    rnd = random.Random(seed)
+    B = {}
+    for name, c in (("kv", 1), ("dq_full", 1), ("dq_free", 256), ("drain", 2)):
+        B[name] = Bar(name, c)
+    for h in range(2):
+        for name, c in (("sp_full", 1), ("p_full", 128), ("stats", 128), ("acc_done", 1)):
+            B[f"{name}{h}"] = Bar(f"{name}{h}", c)
+    for s in range(stages):
+        B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
+        B[f"qd_empty{s}"] = Bar(f"qd_empty{s}", qd_empty_count)
+    # buffer contents
+    stage = [None] * stages                       # block whose Q/dO a stage holds
+    sdp = [None, None]                            # block whose S/dP a half's columns hold
+    pt = [[None] * 4 for _ in range(2)]           # block whose packed P^T a half's warp rows hold
+    ds = [[[None] * 4 for _ in range(2)] for _ in range(2)]  # [buffer][half][warp] -> ("dS"|"stage", block)
+    dq = [None]                                   # block whose dQ the dQ columns hold
+    q1, q2, tma = [], [], []
+
+    def s_mma(i, h):
+        def run():
+            assert stage[i % stages] == i, f"S({i},{h}) reads stage {i % stages} holding {stage[i % stages]}"
+            sdp[h] = i
+        return ("mma", run)
+
+    def acc_mma(i, h):
+        def run():
+            assert stage[i % stages] == i, f"acc({i},{h}) reads stage {i % stages} holding {stage[i % stages]}"
+            assert all(x == i for x in pt[h]), f"dV({i},{h}) reads P^T {pt[h]}"
+            assert all(x == ("dS", i) for x in ds[i & 1][h]), f"dK({i},{h}) reads dS rows {ds[i & 1][h]}"
+        return ("mma", run)
+
+    def dq_mma(i):
+        def run():
+            for h in range(2):
+                assert all(x == ("dS", i) for x in ds[i & 1][h]), f"dQ({i}) reads dS rows {ds[i & 1][h]}"
+            dq[0] = i
+        return ("mma", run)
+
+    def producer():
+        tma.append(("kv", None))
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_empty{s}", it // stages - 1)
+            tma.append((f"qd_full{s}", (s, it)))
+
+    def warp1():
+        yield ("wait", "kv", 0)
+        yield ("wait", "qd_full0", 0)
+        q1.extend([s_mma(0, 0), ("commit", "sp_full0"), s_mma(0, 1), ("commit", "sp_full1"),
+                   ("commit", "qd_empty0")])
+        for it in range(n_it):
+            nxt = it + 1 < n_it
+            yield ("wait", "p_full0", it)
+            if nxt:
+                s1 = (it + 1) % stages
+                yield ("wait", f"qd_full{s1}", (it + 1) // stages)
+                q1.extend([s_mma(it + 1, 0), ("commit", "sp_full0")])
+            yield ("wait", "p_full1", it)
+            if nxt:
+                q1.extend([s_mma(it + 1, 1), ("commit", "sp_full1"), ("commit", f"qd_empty{(it + 1) % stages}")])
+        q1.append(("commit", "drain"))
+        yield ("wait", "drain", 0)
+
+    def warp2():
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", "p_full0", it)
+            if acc_waits_qd:
+                yield ("wait", f"qd_full{s}", it // stages)
+            q2.extend([acc_mma(it, 0), ("commit", "acc_done0")])
+            yield ("wait", "p_full1", it)
+            q2.extend([acc_mma(it, 1), ("commit", "acc_done1"), ("commit", f"qd_empty{s}")])
+            if it > 0 and acc_waits_dq_free:
+                yield ("wait", "dq_free", it - 1)
+            q2.extend([dq_mma(it), ("commit", "dq_full")])
+        q2.append(("commit", "drain"))
+
+    def grads(h, w):
+        def readout(blk):
+            yield ("wait", "dq_full", blk)
+            assert dq[0] == blk, f"readout({blk}) finds dQ of block {dq[0]}"
+            yield ("arrive", "dq_free", 32)
+            # stage this warp's dQ rows in its rows of half h of buffer blk & 1 (the bulk reduction has read
+            # them before the same warp writes there again)
+            assert ds[blk & 1][h][w] == ("dS", blk)
+            ds[blk & 1][h][w] = ("stage", blk)
+        for it in range(n_it):
+            yield ("arrive", f"stats{h}", 32)
+            yield ("wait", f"stats{h}", it)
+            yield ("wait", f"sp_full{h}", it)
+            assert sdp[h] == it, f"pass({it},{h}) reads S/dP of block {sdp[h]}"
+            if it > 0 and acc_waits:
+                yield ("wait", f"acc_done{h}", it - 1)
+            pt[h][w] = it
+            ds[it & 1][h][w] = ("dS", it)
+            yield ("arrive", f"p_full{h}", 32)
+            # S/dP of this half may be overwritten from here on
+            if it > 0:
+                yield from readout(it - 1)
+        yield from readout(n_it - 1)
+
+    agents = {"producer": producer(), "warp1": warp1(), "warp2": warp2()}
+    for h in range(2):
+        for w in range(4):
+            agents[f"g{h}.{w}"] = grads(h, w)
+    waiting = {k: None for k in agents}
+    while agents or q1 or q2 or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        if q1:
+            ready.append("#q1")
+        if q2:
+            ready.append("#q2")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c in ("#q1", "#q2"):
+            q = q1 if c == "#q1" else q2
+            kind, x = q.pop(0)
+            if kind == "mma":
+                x()
+            else:
+                B[x].arrive(1)
+            continue
+        if c == "#tma":
+            name, load = tma.pop(rnd.randrange(len(tma)))
+            if load is not None:
+                stage[load[0]] = load[1]
+            B[name].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

@@ -167,3 +167,23 @@ def test_bk128_mutations_are_caught(mutation):
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 5, 9])
+def test_backward_two_issuer_protocol(n_it):
+    """The d = 64 backward with the S/dP products on one issuing warp and the dV/dK/dQ products on
+    another: every interleaving of the two product queues keeps each buffer's contents right."""
+    from pipeline_model import simulate_bwd_split
+
+    for stages in (2, 3):
+        for seed in range(150):
+            assert simulate_bwd_split(n_it, stages, seed)
+
+
+@pytest.mark.parametrize("mutation", [{"acc_waits": False}, {"qd_empty_count": 1}, {"acc_waits_dq_free": False}])
+def test_backward_two_issuer_mutations_are_caught(mutation):
+    from pipeline_model import Deadlock, simulate_bwd_split
+
+    with pytest.raises((AssertionError, Deadlock)):
+        for seed in range(400):
+            simulate_bwd_split(6, 3, seed, **mutation)
