@@ -17,7 +17,8 @@
 // One CTA owns a 128-key block j of one (b, h) and loops over the 128-row query
 // blocks i that can see it (all of them, or i >= j when causal):
 //   warp 0      TMA: K_j and V_j once, then Q_i and dO_i through a ring
-//   warp 1      MMA issue (warp-uniform loop, lane 0 issues), tcgen05 kind::f16
+//   warps 1, 2  MMA issue (warp-uniform loops, lane 0 issues), tcgen05 kind::f16: warp 1 S^T, dV
+//               and dQ's head columns 0..63, warp 2 dP^T, dK and dQ's columns 64..127
 //   warps 4-11  two warpgroups; thread r of a group owns TMEM lane r. Group g
 //               first turns query columns [64 g, 64 g + 64) of S^T, dP^T into
 //               P^T and dS^T for key r, then reads out dQ for query row r,
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using C = BwdCfg<T, D>;
+    static_assert(D == 128, "the two issuing warps take one 64-column half of dQ each");
     constexpr int ST = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -220,15 +222,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar_kv, 1);
+        // the completion barriers of the products take one commit from each issuing warp
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar_qd_full(s), 1);
-            mbar_init(bar_qd_empty(s), 1);
+            mbar_init(bar_qd_empty(s), 2);
         }
-        mbar_init(bar_sp_full, 1);
+        mbar_init(bar_sp_full, 2);
         mbar_init(bar_p_full, kGradThreads);
-        mbar_init(bar_dq_full, 1);
+        mbar_init(bar_dq_full, 2);
         mbar_init(bar_dq_free, kGradThreads);
-        mbar_init(bar_drain, 1);
+        mbar_init(bar_drain, 2);
         mbar_init(bar_stats, kGradThreads);
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -270,11 +273,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int it = issued - ST > 0 ? issued - ST : 0; it < issued; ++it)
                 bwd_wait(bar_qd_full(it % ST), (it / ST) & 1u, p);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ---------------------------------------------------------------- MMA issuers
+        // One warp issues only about one product every 77 cycles, so the products are split over two
+        // warps: warp 1 issues S^T, dV and dQ's head columns 0..63, warp 2 dP^T, dK and dQ's columns
+        // 64..127. Each product's columns are its own warp's (S^T, packed P^T, dQ half 0 in [0, 128);
+        // dP^T, dS^T, dQ half 1 in [128, 256)); sp_full, dq_full, qd_empty and drain take a commit from
+        // each warp, and each warp waits dq_free (every product of the last block done and dQ read
+        // out) before its next S^T or dP^T overwrites its columns.
+        const int h = warp - 1;  // 0: S^T, dV, dQ half 0; 1: dP^T, dK, dQ half 1
         const uint32_t issue = lane == 0 ? 1u : 0u;
-        const uint64_t k_km = smem_desc_sw128(smem_u32(smem + C::SMEM_K), 16, 1024);         // K_j as A, K-major
-        const uint64_t v_km = smem_desc_sw128(smem_u32(smem + C::SMEM_V), 16, 1024);         // V_j as A, K-major
+        const uint64_t a_km = smem_desc_sw128(smem_u32(smem + (h == 0 ? C::SMEM_K : C::SMEM_V)), 16, 1024);
         const uint64_t k_mn = smem_desc_sw128(smem_u32(smem + C::SMEM_K), C::CHUNK, 1024);   // K_j as B, N-major
         const uint64_t ds_mn = smem_desc_sw128(smem_u32(smem + C::SMEM_DS), C::CHUNK, 1024); // dS as A, M-major
         bool ok = bwd_wait_warp(bar_kv, 0, p);
@@ -285,46 +294,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t q_s = smem_u32(smem + C::SMEM_QD + s * 2 * C::TILE);
-            const uint64_t q_km = smem_desc_sw128(q_s, 16, 1024);
-            const uint64_t do_km = smem_desc_sw128(q_s + C::TILE, 16, 1024);
-            const uint64_t q_mn = smem_desc_sw128(q_s, C::CHUNK, 1024);
-            const uint64_t do_mn = smem_desc_sw128(q_s + C::TILE, C::CHUNK, 1024);
-            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T, contracted over the head dimension
+            // B of S^T is Q_i, of dP^T dO_i (K-major); B of dV is dO_i, of dK Q_i (N-major)
+            const uint64_t b_km = smem_desc_sw128(q_s + (h == 0 ? 0 : C::TILE), 16, 1024);
+            const uint64_t b_mn = smem_desc_sw128(q_s + (h == 0 ? C::TILE : 0), C::CHUNK, 1024);
+            // S^T = K_j Q_i^T (h = 0) or dP^T = V_j dO_i^T (h = 1), contracted over the head dimension
 #pragma unroll
             for (int k = 0; k < C::KSTEPS_D; ++k) {
                 const uint64_t off = (uint64_t)(((k / 4) * C::CHUNK + (k % 4) * 32) >> 4);
-                mma_ss(tmem + 0, k_km + off, q_km + off, C::ID_ST, k > 0 ? 1u : 0u, issue);
-                mma_ss(tmem + 128, v_km + off, do_km + off, C::ID_ST, k > 0 ? 1u : 0u, issue);
+                mma_ss(tmem + 128 * h, a_km + off, b_km + off, C::ID_ST, k > 0 ? 1u : 0u, issue);
             }
             tc_commit(bar_sp_full, issue);
             ok = bwd_wait_warp(bar_p_full, it & 1u, p);
             if (!ok) break;
             tc_fence_after();
-            // dV_j += P^T dO_i and dK_j += dS^T Q_i, contracted over the 128 query rows
+            // dV_j += P^T dO_i (h = 0) or dK_j += dS^T Q_i (h = 1), contracted over the 128 query rows
 #pragma unroll
             for (int k = 0; k < C::KSTEPS_R; ++k) {
                 const uint64_t off = (uint64_t)((k * 2048) >> 4);
                 const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
                 const uint32_t pcol = (uint32_t)(k < 4 ? 8 * k : 64 + 8 * k);  // packed P^T / dS^T of queries 16k..
-                mma_ts(tmem + 256, tmem + 0 + pcol, do_mn + off, C::ID_ACC, acc, issue);
-                mma_ts(tmem + 256 + D, tmem + 128 + pcol, q_mn + off, C::ID_ACC, acc, issue);
+                mma_ts(tmem + 256 + D * h, tmem + 128 * h + pcol, b_mn + off, C::ID_ACC, acc, issue);
             }
-            // dQ_i = dS K_j, contracted over the 128 keys, 64 head columns at a time; the halves'
-            // accumulation chains are interleaved (a chain completes about one product per 77 cycles)
+            // dQ_i = dS K_j, contracted over the 128 keys, head columns 64h..64h+63
 #pragma unroll
-            for (int k = 0; k < C::KSTEPS_R; ++k)
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    const uint64_t off = (uint64_t)((k * 2048) >> 4);
-                    mma_ss(tmem + (h == 0 ? 32 : 160), ds_mn + off, k_mn + (uint64_t)((h * C::CHUNK) >> 4) + off,
-                           C::ID_DQ, k > 0 ? 1u : 0u, issue);
-                }
+            for (int k = 0; k < C::KSTEPS_R; ++k) {
+                const uint64_t off = (uint64_t)((k * 2048) >> 4);
+                mma_ss(tmem + (h == 0 ? 32 : 160), ds_mn + off, k_mn + (uint64_t)((h * C::CHUNK) >> 4) + off,
+                       C::ID_DQ, k > 0 ? 1u : 0u, issue);
+            }
             tc_commit(bar_dq_full, issue);
             tc_commit(bar_qd_empty(s), issue);
         }
-        // Every MMA this warp issued is complete before tensor memory is freed.
+        // Every MMA of both warps is complete before tensor memory is freed.
         tc_commit(bar_drain, issue);
-        bwd_wait_warp(bar_drain, 0, p);
+        if (warp == 1) bwd_wait_warp(bar_drain, 0, p);
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- gradient warps
         const int g = (warp - 4) >> 2;             // warpgroup: query columns / head columns half g

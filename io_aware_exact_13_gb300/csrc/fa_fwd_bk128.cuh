@@ -8,12 +8,11 @@
 // their running (m, l, a); K/V blocks stream past them; S, P and O live in
 // tensor memory; only O and lse are written.
 //
-// Why 128-key blocks: a chain of tcgen05.mma products accumulating into one
-// accumulator completes about one product every 77 cycles whatever its size,
-// and products into other accumulators (another chain of the same warp, or
-// another warp's) fill the gap: with two or more chains an M=128 K=16 product
-// with N = 128 takes 64 cycles, the full rate, and one with N = 64 takes 48
-// (its shared-memory operands are the limit, 67 % of the rate). So S = Q K^T
+// Why 128-key blocks: one warp issues about one tcgen05.mma every 77-84 cycles
+// whatever its size, even alternating between several accumulators, and the
+// tensor core keeps up with two or more issuing warps: an M=128 K=16 product
+// with N = 128 takes 64 cycles at the full rate, one with N = 64 takes 48 (its
+// shared-memory operands are the limit, 67 % of the rate). So S = Q K^T
 // products over 128 keys cost half the tensor time per flop of 64-key ones.
 //
 // Tensor memory (512 columns) holds ONE S buffer that the two tiles use in turn

@@ -827,3 +827,124 @@ def simulate_bwd_split(n_it, stages, seed, acc_waits=True, qd_empty_count=2, acc
             del agents[c]
             waiting[c] = None
     return True
+
+
+def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_count=2, waits_dq_free=True):
+    """The d = 128 backward with two issuing warps: warp 1 issues S^T, dV and dQ's first 64 head
+    columns, warp 2 dP^T, dK and dQ's second half; each warp's products run in order in their own
+    queue. The tensor-memory columns alias (S^T, then packed P^T and dQ half 0 in [0, 128); dP^T,
+    then dS^T and dQ half 1 in [128, 256)), so the model tracks which block each holds: a product
+    that overwrites columns before their last reader, or a reader that finds the wrong block,
+    fails. Completion barriers count a commit from each warp (sp_full, dq_full, qd_empty, drain).
+    Mutations that must be caught: sp_count=1, dq_count=1, qd_empty_count=1, waits_dq_free=False."""
+    rnd = random.Random(seed)
+    B = {}
+    n = 256
+    for name, c in (("kv", 1), ("sp_full", sp_count), ("p_full", n), ("dq_full", dq_count), ("dq_free", n),
+                    ("drain", 2), ("stats", n)):
+        B[name] = Bar(name, c)
+    for s in range(stages):
+        B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
+        B[f"qd_empty{s}"] = Bar(f"qd_empty{s}", qd_empty_count)
+    stage = [None] * stages
+    # per half of the tensor memory (0: S^T side, 1: dP^T side): what the columns hold
+    cols = [{"sdp": None, "packed": None, "dq": None} for _ in range(2)]
+    packed_read = [None, None]   # last block whose packed P^T / dS^T the dV / dK product read
+    dq_read = [set(), set()]      # (block, warp) pairs that read dQ half h out
+    ds_smem = [None]              # ("dS" | "stage", block) of the shared-memory dS buffer
+    qs = [[], []]
+    tma = []
+
+    def prod(h, kind, i):
+        def run():
+            assert stage[i % stages] == i, f"{kind}({i}) reads stage {i % stages} holding {stage[i % stages]}"
+            c = cols[h]
+            if kind == "sdp":
+                if i > 0:
+                    assert packed_read[h] == i - 1, f"S/dP({i}) over packed columns dV/dK({i - 1}) did not read"
+                    assert all((i - 1, w) in dq_read[h] for w in range(8)), f"S/dP({i}) over dQ({i - 1}) half {h}"
+                c["sdp"] = i
+            elif kind == "acc":
+                assert c["packed"] == i, f"dV/dK({i}) half {h} reads packed block {c['packed']}"
+                packed_read[h] = i
+            else:  # dq
+                assert ds_smem[0] == ("dS", i), f"dQ({i}) reads dS {ds_smem[0]}"
+                c["dq"] = i
+        return ("mma", run)
+
+    def producer():
+        tma.append(("kv", None))
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_empty{s}", it // stages - 1)
+            tma.append((f"qd_full{s}", (s, it)))
+
+    def issuer(h):
+        yield ("wait", "kv", 0)
+        for it in range(n_it):
+            s = it % stages
+            yield ("wait", f"qd_full{s}", it // stages)
+            if it > 0 and waits_dq_free:
+                yield ("wait", "dq_free", it - 1)
+            qs[h].extend([prod(h, "sdp", it), ("commit", "sp_full")])
+            yield ("wait", "p_full", it)
+            qs[h].extend([prod(h, "acc", it), prod(h, "dq", it), ("commit", "dq_full"), ("commit", f"qd_empty{s}")])
+        qs[h].append(("commit", "drain"))
+        if h == 0:
+            yield ("wait", "drain", 0)
+
+    def grads(w):
+        for it in range(n_it):
+            yield ("arrive", "stats", 32)
+            yield ("wait", "stats", it)
+            yield ("wait", "sp_full", it)
+            assert cols[0]["sdp"] == it and cols[1]["sdp"] == it, f"pass({it}) finds S/dP {cols[0]['sdp']}, {cols[1]['sdp']}"
+            cols[0]["packed"] = cols[1]["packed"] = it
+            ds_smem[0] = ("dS", it)
+            yield ("arrive", "p_full", 32)
+            yield ("wait", "dq_full", it)
+            assert cols[0]["dq"] == it and cols[1]["dq"] == it, f"readout({it}) finds dQ {cols[0]['dq']}, {cols[1]['dq']}"
+            dq_read[0].add((it, w))
+            dq_read[1].add((it, w))
+            yield ("arrive", "dq_free", 32)
+            ds_smem[0] = ("stage", it)
+
+    agents = {"producer": producer(), "w1": issuer(0), "w2": issuer(1)}
+    for w in range(8):
+        agents[f"g{w}"] = grads(w)
+    waiting = {k: None for k in agents}
+    while agents or qs[0] or qs[1] or tma:
+        ready = [k for k in agents if waiting[k] is None or B[waiting[k][1]].done(waiting[k][2])]
+        for h in range(2):
+            if qs[h]:
+                ready.append(f"#q{h}")
+        if tma:
+            ready.append("#tma")
+        if not ready:
+            raise Deadlock(f"deadlock: {[(k, waiting[k]) for k in agents]}")
+        c = rnd.choice(ready)
+        if c.startswith("#q"):
+            kind, x = qs[int(c[2])].pop(0)
+            if kind == "mma":
+                x()
+            else:
+                B[x].arrive(1)
+            continue
+        if c == "#tma":
+            name, load = tma.pop(rnd.randrange(len(tma)))
+            if load is not None:
+                stage[load[0]] = load[1]
+            B[name].arrive(1)
+            continue
+        try:
+            while True:
+                ev = next(agents[c])
+                if ev[0] == "arrive":
+                    B[ev[1]].arrive(ev[2])
+                    continue
+                waiting[c] = ev
+                break
+        except StopIteration:
+            del agents[c]
+            waiting[c] = None
+    return True

@@ -187,3 +187,24 @@ def test_backward_two_issuer_mutations_are_caught(mutation):
     with pytest.raises((AssertionError, Deadlock)):
         for seed in range(400):
             simulate_bwd_split(6, 3, seed, **mutation)
+
+
+@pytest.mark.parametrize("n_it", [1, 2, 3, 6])
+def test_backward_d128_two_issuer_protocol(n_it):
+    """The d = 128 backward with S^T, dV, dQ's first half on one issuing warp and dP^T, dK, dQ's second
+    half on another: the aliased tensor-memory columns always hold the block their reader expects."""
+    from pipeline_model import simulate_bwd128_split
+
+    for stages in (2, 3):
+        for seed in range(150):
+            assert simulate_bwd128_split(n_it, stages, seed)
+
+
+@pytest.mark.parametrize("mutation", [{"sp_count": 1}, {"dq_count": 1}, {"qd_empty_count": 1},
+                                      {"waits_dq_free": False}])
+def test_backward_d128_two_issuer_mutations_are_caught(mutation):
+    from pipeline_model import Deadlock, simulate_bwd128_split
+
+    with pytest.raises((AssertionError, Deadlock)):
+        for seed in range(400):
+            simulate_bwd128_split(5, 2, seed, **mutation)
