@@ -135,8 +135,11 @@ __device__ __forceinline__ float2 up2(uint32_t v) {
 // pairs to the 16-bit input type: P = 2^(S * scale * log2 e - lse * log2 e) and
 // dS = P (dP - D). neg_l and neg_d are shared-memory addresses of -lse*log2e and
 // -D for the 32 columns (the same for every lane: broadcast loads). Keys past
-// the end, and (causal) keys after the query, get P = dS = 0.
-template <typename T, bool CAUSAL>
+// the end, and (causal) keys after the query, get P = dS = 0 when need_mask is
+// set. MASKING = false compiles a copy without that code, for the blocks that
+// need none: in the causal kernels the masking code kept in the common path
+// cost 30-40 registers and about a fifth of the time per block.
+template <typename T, bool CAUSAL, bool MASKING>
 __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[32], const uint32_t (&dpv)[32], uint32_t neg_l,
                                            uint32_t neg_d, float scale_log2, bool need_mask, bool key_ok, int key,
                                            int q_first, uint32_t (&pp)[16], uint32_t (&dsp)[16]) {
@@ -150,7 +153,7 @@ __device__ __forceinline__ void p_ds_chunk(const uint32_t (&sv)[32], const uint3
                                    make_float2(scale_log2, scale_log2),
                                    h == 0 ? make_float2(nl.x, nl.y) : make_float2(nl.z, nl.w));
             float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (need_mask) {
+            if (MASKING && need_mask) {
                 const int q0 = q_first + c + h;
                 const bool v0 = key_ok && (!CAUSAL || key <= q0);
                 const bool v1 = key_ok && (!CAUSAL || key <= q0 + 1);
@@ -363,8 +366,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_wait(tmem + lane_base + c0, sv, tmem + lane_base + 128 + c0, dpv);
                 uint32_t pp[16], dsp[16];
-                p_ds_chunk<T, CAUSAL>(sv, dpv, stats + c0 * 4, stats + (128 + c0) * 4, p.scale_log2, need_mask, key_ok,
-                                      key, row0 + c0, pp, dsp);
+                if (CAUSAL && !need_mask)  // (a separate copy gained nothing without causal masking)
+                    p_ds_chunk<T, CAUSAL, false>(sv, dpv, stats + c0 * 4, stats + (128 + c0) * 4, p.scale_log2, false,
+                                                 key_ok, key, row0 + c0, pp, dsp);
+                else
+                    p_ds_chunk<T, CAUSAL, true>(sv, dpv, stats + c0 * 4, stats + (128 + c0) * 4, p.scale_log2,
+                                                need_mask, key_ok, key, row0 + c0, pp, dsp);
                 // P^T and dS^T overwrite columns this warpgroup has already read.
                 tmem_st16(tmem + lane_base + 0 + pcol, pp);
                 tmem_st16(tmem + lane_base + 128 + pcol, dsp);
@@ -737,8 +744,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_wait(s_col + c0, sv, s_col + 64 + c0, dpv);
                 uint32_t pp[16], dsp[16];
-                p_ds_chunk<T, CAUSAL>(sv, dpv, stats + c0 * 4, stats + (64 + c0) * 4, p.scale_log2, need_mask,
-                                      key_ok, key, i * kBlk + 64 * g + c0, pp, dsp);
+                if (need_mask)
+                    p_ds_chunk<T, CAUSAL, true>(sv, dpv, stats + c0 * 4, stats + (64 + c0) * 4, p.scale_log2, true,
+                                                key_ok, key, i * kBlk + 64 * g + c0, pp, dsp);
+                else
+                    p_ds_chunk<T, CAUSAL, false>(sv, dpv, stats + c0 * 4, stats + (64 + c0) * 4, p.scale_log2, false,
+                                                 key_ok, key, i * kBlk + 64 * g + c0, pp, dsp);
                 tmem_st16(tmem + lane_base + 256u + 32u * g + c0 / 2, pp);  // packed P^T of half g
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
