@@ -377,6 +377,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_st16(tmem + lane_base + 128 + pcol, dsp);
                 // dS row of key r: queries c0..c0+31 = 64 bytes of chunk g, 128-byte swizzle
                 const uint32_t ds_row = ds_base + g * C::CHUNK + r * 128;
+                if (step == 0) {  // the previous block's dQ reductions, staged in these rows, must have read them
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t unit = (uint32_t)(((c0 % 64) / 8 + u) ^ (r & 7));
@@ -425,9 +429,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     bulk_commit_group();
                 }
             }
-            // the staging area is this warp's dS rows: free it before the next block writes dS
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
         }
         if (lane == 0) bulk_wait_all();
         // ---------------------------------------------------------------- dV_j (group 0), dK_j (group 1)
