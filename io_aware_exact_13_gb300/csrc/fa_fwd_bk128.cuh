@@ -176,8 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(!(DROP && (VARLEN || MASK)), "dropout with dense unmasked inputs only");
     using C = Cfg128<T, D>;
     constexpr int RK = C::RK, RV = C::RV;
-    if constexpr (MASK) {  // the mask had other values: the 64-key kernel applies it as given
-        if (*p.mask_kind != 0) return;
+    if constexpr (MASK) {
+        grid_dependency_wait();  // launched behind the packing pass: its verdict and bits
+        if (*p.mask_kind != 0) return;  // the mask had other values: the 64-key kernel applies it as given
         grid_launch_dependents();  // that kernel (queued next) may take the SMs this grid leaves idle
     }
     extern __shared__ uint8_t smem_raw[];
@@ -531,20 +532,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 sl2v = make_float2(sl2, sl2), negv = make_float2(neg, neg);
                 float2 ls[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                                 make_float2(0.0f, 0.0f)};
-                // P in two halves of 64 keys (32 packed columns each), each stored as soon as it is ready
+                // P in chunks of 2 PC keys (PC packed columns), each stored as soon as it is ready: halves, or
+                // quarters in the masked variants, whose mask registers would not fit beside a half
+                constexpr int PC = MASK ? 16 : 32;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pv[32];
+                for (int qq = 0; qq < 64 / PC; ++qq) {
+                    uint32_t pv[PC];
                     if constexpr (DROP) {
 #pragma unroll
-                        for (int gq = 0; gq < 2; ++gq) {  // 32-key groups: one Philox block each
+                        for (int gq = 0; gq < PC / 16; ++gq) {  // 32-key groups: one Philox block each
                             uint32_t kw[8];
-                            philox4x64_10((uint64_t)row, (uint64_t)(4 * j + 2 * hh + gq), (uint64_t)bh, p.drop_offset,
-                                          p.drop_seed, 0ull, kw);
+                            philox4x64_10((uint64_t)row, (uint64_t)(4 * j + (PC / 16) * qq + gq), (uint64_t)bh,
+                                          p.drop_offset, p.drop_seed, 0ull, kw);
 #pragma unroll
                             for (int c2 = 0; c2 < 16; ++c2) {
                                 const int c = 16 * gq + c2;
-                                const int i = 64 * hh + 2 * c;
+                                const int i = 2 * PC * qq + 2 * c;
                                 const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
                                 const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                                 ls[c & 3] = fadd2(ls[c & 3], e);  // the row sum is of the undropped scores
@@ -556,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            const int i = 64 * hh + 2 * c;
+                        for (int c = 0; c < PC; ++c) {
+                            const int i = 2 * PC * qq + 2 * c;
                             const float2 a = ffma2(make_float2(x[i], x[i + 1]), sl2v, negv);
                             const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
                             ls[c & 3] = fadd2(ls[c & 3], e);
@@ -566,12 +569,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // P V(g-1), the tile's previous product, read P_t and accumulated into O_t:
                     // wait for its commit before overwriting P_t (and before rescaling O_t below).
-                    if (hh == 0 && g > 0) {
+                    if (qq == 0 && g > 0) {
                         ok = wait_warp(sy.pv_done(t, (g - 1) & 1u), ((g - 1) >> 1) & 1u, abort_flag, p);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    tmem_st32(p_addr + 32 * hh, pv);
+                    if constexpr (PC == 16)
+                        tmem_st16(p_addr + 16 * qq, pv);
+                    else
+                        tmem_st32(p_addr + 32 * qq, pv);
                 }
                 if (!ok) break;
                 l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));

@@ -21,6 +21,7 @@
 #include <cstdint>
 
 #include "fa_launch.cuh"
+#include "pdl.cuh"
 
 namespace fa {
 
@@ -52,6 +53,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kPackThreads) fa_mask_pack_kernel(const float *__restrict__ mask,
                                                                     uint4 *__restrict__ bits, int *__restrict__ kind,
                                                                     long long rows, int nk, int nblk) {
+    grid_launch_dependents();  // the 128-key kernel may be scheduled; it waits for this grid to finish
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
