@@ -37,12 +37,16 @@
 //   [256,256+d) dV_j accumulator,  [256+d,256+2d) dK_j accumulator
 // dV_j += P^T dO_i and dK_j += dS^T Q_i take A from tensor memory; dQ_i = dS K_j
 // takes A = dS from shared memory, written by the gradient warps with the
-// query index contiguous (an M-major operand). Each warp then stages its
-// 32 x 32 fp32 tiles of dQ_i in its own part of that dS buffer and adds them
-// into an fp32 workspace with bulk tensor reductions (reduce-add in L2); a
-// last kernel converts the workspace to the output type. The row statistics
-// of block i (lse * log2 e and D, padded past N) are loaded one iteration
-// ahead and handed over in shared memory.
+// query index contiguous (an M-major operand). Each warp then stages its two
+// 32 x 32 fp32 tiles of dQ_i, one in its own part of that dS buffer and one
+// in the dO half of block i's stage (dead once every product of the block is
+// done), and adds them into an fp32 workspace with bulk tensor reductions
+// (reduce-add in L2); a last kernel converts the workspace to the output type.
+// So a stage's Q and dO halves have their own barriers: Q goes back to the
+// producer by the issuing warps' commits, dO by the gradient warps once their
+// reductions have read the tiles, which they wait for before the next pass
+// writes dS. The row statistics of block i (lse * log2 e and D, padded past N)
+// are loaded one iteration ahead and handed over in shared memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -74,7 +78,7 @@ struct BwdCfg {
     static constexpr int SMEM_DS = SMEM_QD + STAGES * 2 * TILE;  // dS: 2 chunks (queries 0-63, 64-127) x 128 keys
     static constexpr int SMEM_STATS = SMEM_DS + 2 * CHUNK;       // -lse2[128], -D[128] of the current block
     static constexpr int SMEM_BAR = SMEM_STATS + 256 * 4;
-    static constexpr int NUM_BARS = 1 + 2 * STAGES + 6;
+    static constexpr int NUM_BARS = 1 + 4 * STAGES + 6;
     static constexpr int SMEM_BYTES = SMEM_BAR + NUM_BARS * 8 + 16 + 1024;
     static constexpr uint32_t FMT = Elem<T>::fmt;
     static constexpr uint32_t ID_ST = make_idesc_ab(FMT, 128, 128, 0, 0);  // S^T, dP^T: A, B K-major
@@ -203,14 +207,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::SMEM_BAR);
     const uint32_t bar_kv = smem_u32(bars);
-    auto bar_qd_full = [&](int s) { return smem_u32(bars + 1 + s); };
-    auto bar_qd_empty = [&](int s) { return smem_u32(bars + 1 + ST + s); };
-    const uint32_t bar_sp_full = smem_u32(bars + 1 + 2 * ST);  // S^T, dP^T in TMEM
-    const uint32_t bar_p_full = smem_u32(bars + 2 + 2 * ST);   // P^T, dS^T, dS written (256 arrivals)
-    const uint32_t bar_dq_full = smem_u32(bars + 3 + 2 * ST);  // every product of the iteration done
-    const uint32_t bar_dq_free = smem_u32(bars + 4 + 2 * ST);  // dQ loaded from TMEM (256 arrivals)
-    const uint32_t bar_drain = smem_u32(bars + 5 + 2 * ST);    // all issued MMAs done (exit)
-    const uint32_t bar_stats = smem_u32(bars + 6 + 2 * ST);    // row statistics of the block stored (256 arrivals)
+    auto bar_q_full = [&](int s) { return smem_u32(bars + 1 + s); };
+    auto bar_q_empty = [&](int s) { return smem_u32(bars + 1 + ST + s); };       // both warps' last Q reader
+    auto bar_do_full = [&](int s) { return smem_u32(bars + 1 + 2 * ST + s); };
+    auto bar_do_empty = [&](int s) { return smem_u32(bars + 1 + 3 * ST + s); };  // dQ tiles staged there read
+    const uint32_t bar_sp_full = smem_u32(bars + 1 + 4 * ST);  // S^T, dP^T in TMEM
+    const uint32_t bar_p_full = smem_u32(bars + 2 + 4 * ST);   // P^T, dS^T, dS written (256 arrivals)
+    const uint32_t bar_dq_full = smem_u32(bars + 3 + 4 * ST);  // every product of the iteration done
+    const uint32_t bar_dq_free = smem_u32(bars + 4 + 4 * ST);  // dQ loaded from TMEM (256 arrivals)
+    const uint32_t bar_drain = smem_u32(bars + 5 + 4 * ST);    // all issued MMAs done (exit)
+    const uint32_t bar_stats = smem_u32(bars + 6 + 4 * ST);    // row statistics of the block stored (256 arrivals)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::SMEM_BAR + C::NUM_BARS * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -227,8 +233,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar_kv, 1);
         // the completion barriers of the products take one commit from each issuing warp
         for (int s = 0; s < ST; ++s) {
-            mbar_init(bar_qd_full(s), 1);
-            mbar_init(bar_qd_empty(s), 2);
+            mbar_init(bar_q_full(s), 1);
+            mbar_init(bar_q_empty(s), 2);
+            mbar_init(bar_do_full(s), 1);
+            mbar_init(bar_do_empty(s), kGradThreads / 32);  // one arrival per gradient warp
         }
         mbar_init(bar_sp_full, 2);
         mbar_init(bar_p_full, kGradThreads);
@@ -257,24 +265,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(smem_u32(smem + C::SMEM_K + c * C::CHUNK), &tm_k, bar_kv, c * 64, j * kBlk, bh, pol);
                 tma_load_3d(smem_u32(smem + C::SMEM_V + c * C::CHUNK), &tm_v, bar_kv, c * 64, j * kBlk, bh, pol);
             }
-            int issued = 0;
+            int issued_q = 0, issued_do = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int s = it % ST;
-                if (!bwd_wait(bar_qd_empty(s), ((it / ST) & 1u) ^ 1u, p)) break;
                 const uint32_t dst = smem_u32(smem + C::SMEM_QD + s * 2 * C::TILE);
-                mbar_arrive_expect_tx(bar_qd_full(s), 2 * C::TILE);
                 const int row0 = (i0 + it) * kBlk;
-                for (int c = 0; c < C::NCH; ++c) {
-                    tma_load_3d(dst + c * C::CHUNK, &tm_q, bar_qd_full(s), c * 64, row0, bh, pol);
-                    tma_load_3d(dst + C::TILE + c * C::CHUNK, &tm_do, bar_qd_full(s), c * 64, row0, bh, pol);
-                }
-                issued = it + 1;
+                if (!bwd_wait(bar_q_empty(s), ((it / ST) & 1u) ^ 1u, p)) break;
+                mbar_arrive_expect_tx(bar_q_full(s), C::TILE);
+                for (int c = 0; c < C::NCH; ++c) tma_load_3d(dst + c * C::CHUNK, &tm_q, bar_q_full(s), c * 64, row0, bh, pol);
+                issued_q = it + 1;
+                // dO's half also held the dQ tiles of the stage's last block until they were read
+                if (!bwd_wait(bar_do_empty(s), ((it / ST) & 1u) ^ 1u, p)) break;
+                mbar_arrive_expect_tx(bar_do_full(s), C::TILE);
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_3d(dst + C::TILE + c * C::CHUNK, &tm_do, bar_do_full(s), c * 64, row0, bh, pol);
+                issued_do = it + 1;
             }
             // Before the CTA may exit, every copy into its shared memory must have
             // landed (they all have on the normal path; this matters after a timeout).
             bwd_wait(bar_kv, 0, p);
-            for (int it = issued - ST > 0 ? issued - ST : 0; it < issued; ++it)
-                bwd_wait(bar_qd_full(it % ST), (it / ST) & 1u, p);
+            for (int it = issued_q - ST > 0 ? issued_q - ST : 0; it < issued_q; ++it)
+                bwd_wait(bar_q_full(it % ST), (it / ST) & 1u, p);
+            for (int it = issued_do - ST > 0 ? issued_do - ST : 0; it < issued_do; ++it)
+                bwd_wait(bar_do_full(it % ST), (it / ST) & 1u, p);
         }
     } else if (warp == 1 || warp == 2) {
         // ---------------------------------------------------------------- MMA issuers
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = bwd_wait_warp(bar_kv, 0, p);
         for (int it = 0; ok && it < n_it; ++it) {
             const int s = it % ST;
-            ok = bwd_wait_warp(bar_qd_full(s), (it / ST) & 1u, p);
+            ok = bwd_wait_warp(bar_q_full(s), (it / ST) & 1u, p) && bwd_wait_warp(bar_do_full(s), (it / ST) & 1u, p);
             if (ok && it > 0) ok = bwd_wait_warp(bar_dq_free, (it - 1) & 1u, p);
             if (!ok) break;
             tc_fence_after();
@@ -326,7 +339,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        C::ID_DQ, k > 0 ? 1u : 0u, issue);
             }
             tc_commit(bar_dq_full, issue);
-            tc_commit(bar_qd_empty(s), issue);
+            tc_commit(bar_q_empty(s), issue);  // dO's half is released by the gradient warps
         }
         // Every MMA of both warps is complete before tensor memory is freed.
         tc_commit(bar_drain, issue);
@@ -377,8 +390,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_st16(tmem + lane_base + 128 + pcol, dsp);
                 // dS row of key r: queries c0..c0+31 = 64 bytes of chunk g, 128-byte swizzle
                 const uint32_t ds_row = ds_base + g * C::CHUNK + r * 128;
-                if (step == 0) {  // the previous block's dQ reductions, staged in these rows, must have read them
-                    if (lane == 0) bulk_wait_read_all();
+                if (step == 0) {  // the previous block's dQ reductions (staged in these rows and in the dO half
+                                  // of its stage) must have read them; that dO half goes back to the producer
+                    if (lane == 0) {
+                        bulk_wait_read_all();
+                        if (it > 0) mbar_arrive(bar_do_empty((it - 1) % ST));
+                    }
                     __syncwarp();
                 }
 #pragma unroll
@@ -409,15 +426,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(bar_dq_free);
+            // tile 0 in this warp's dS rows, tile 1 in the dO half of the block's stage (every product of the
+            // block is done: dq_full)
+            const uint32_t stage1 = smem_u32(smem + C::SMEM_QD + (it % ST) * 2 * C::TILE + C::TILE) + (g * 4 + w) * 4096;
 #pragma unroll
             for (int t = 0; t < COLS / 32; ++t) {
-                if (t > 0) {  // the previous tile's reduction must have read the staging area
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-                }
+                const uint32_t box = t == 0 ? stage : stage1;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) * 16),
+                    st_shared_v4(box + lane * 128 + ((u ^ (lane & 7)) * 16),
                                  __float_as_uint(__uint_as_float(qv[32 * t + 4 * u]) * p.scale),
                                  __float_as_uint(__uint_as_float(qv[32 * t + 4 * u + 1]) * p.scale),
                                  __float_as_uint(__uint_as_float(qv[32 * t + 4 * u + 2]) * p.scale),
@@ -425,12 +442,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_reduce_add_3d(&tm_dq, stage, g * COLS + 32 * t, row0 + w * 32, bh);
+                    tma_reduce_add_3d(&tm_dq, box, g * COLS + 32 * t, row0 + w * 32, bh);
                     bulk_commit_group();
                 }
             }
         }
-        if (lane == 0) bulk_wait_all();
         // ---------------------------------------------------------------- dV_j (group 0), dK_j (group 1)
         // The last dq_full completion covers every dV and dK product (a commit
         // tracks all earlier MMAs of the issuing thread).
@@ -459,6 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();  // the dQ reductions, behind the dV / dK stores
     }
     __syncwarp();
     tc_fence_before();
@@ -766,7 +783,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (it > 0) ok = readout(i - 1);
         }
         if (ok) ok = readout(i0 + n_it - 1);
-        if (lane == 0) bulk_wait_all();
         // ---------------------------------------------------------------- dV_j (half A's group), dK_j (B's)
         if (ok) {  // the last dq_full covers every dV and dK product
             tc_fence_after();
@@ -788,6 +804,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();  // the dQ reductions, behind the dV / dK stores
     }
     __syncwarp();
     tc_fence_before();

@@ -829,14 +829,21 @@ def simulate_bwd_split(n_it, stages, seed, acc_waits=True, qd_empty_count=2, acc
     return True
 
 
-def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_count=2, waits_dq_free=True):
+def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, q_empty_count=2, waits_dq_free=True,
+                          do_empty_count=8, release_after_read=True):
     """The d = 128 backward with two issuing warps: warp 1 issues S^T, dV and dQ's first 64 head
     columns, warp 2 dP^T, dK and dQ's second half; each warp's products run in order in their own
     queue. The tensor-memory columns alias (S^T, then packed P^T and dQ half 0 in [0, 128); dP^T,
     then dS^T and dQ half 1 in [128, 256)), so the model tracks which block each holds: a product
     that overwrites columns before their last reader, or a reader that finds the wrong block,
-    fails. Completion barriers count a commit from each warp (sp_full, dq_full, qd_empty, drain).
-    Mutations that must be caught: sp_count=1, dq_count=1, qd_empty_count=1, waits_dq_free=False."""
+    fails. Completion barriers count a commit from each warp (sp_full, dq_full, q_empty, drain).
+    A stage's Q and dO halves have their own barriers: Q goes back to the producer by the issuing
+    warps' commits, dO by the eight gradient warps, because each stages its second dQ tile there
+    (its first in its own dS rows) and releases it once its bulk reductions have read it, which it
+    waits for at its next pass. The model keeps those reads pending until that wait, so a dO copy
+    landing on a tile not yet read fails.
+    Mutations that must be caught: sp_count=1, dq_count=1, q_empty_count=1, waits_dq_free=False,
+    do_empty_count=7, release_after_read=False (released when staged)."""
     rnd = random.Random(seed)
     B = {}
     n = 256
@@ -844,9 +851,12 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
                     ("drain", 2), ("stats", n)):
         B[name] = Bar(name, c)
     for s in range(stages):
-        B[f"qd_full{s}"] = Bar(f"qd_full{s}", 1)
-        B[f"qd_empty{s}"] = Bar(f"qd_empty{s}", qd_empty_count)
-    stage = [None] * stages
+        B[f"q_full{s}"] = Bar(f"q_full{s}", 1)
+        B[f"q_empty{s}"] = Bar(f"q_empty{s}", q_empty_count)
+        B[f"do_full{s}"] = Bar(f"do_full{s}", 1)
+        B[f"do_empty{s}"] = Bar(f"do_empty{s}", do_empty_count)
+    stage_q, stage_do = [None] * stages, [None] * stages
+    do_tiles = [set() for _ in range(stages)]  # warps whose dQ tile in a stage's dO half is not read yet
     # per half of the tensor memory (0: S^T side, 1: dP^T side): what the columns hold
     cols = [{"sdp": None, "packed": None, "dq": None} for _ in range(2)]
     packed_read = [None, None]   # last block whose packed P^T / dS^T the dV / dK product read
@@ -857,7 +867,8 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
 
     def prod(h, kind, i):
         def run():
-            assert stage[i % stages] == i, f"{kind}({i}) reads stage {i % stages} holding {stage[i % stages]}"
+            s = i % stages
+            assert stage_q[s] == i and stage_do[s] == i, f"{kind}({i}) reads stage {s}: Q {stage_q[s]}, dO {stage_do[s]}"
             c = cols[h]
             if kind == "sdp":
                 if i > 0:
@@ -876,19 +887,22 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
         tma.append(("kv", None))
         for it in range(n_it):
             s = it % stages
-            yield ("wait", f"qd_empty{s}", it // stages - 1)
-            tma.append((f"qd_full{s}", (s, it)))
+            yield ("wait", f"q_empty{s}", it // stages - 1)
+            tma.append((f"q_full{s}", ("q", s, it)))
+            yield ("wait", f"do_empty{s}", it // stages - 1)
+            tma.append((f"do_full{s}", ("do", s, it)))
 
     def issuer(h):
         yield ("wait", "kv", 0)
         for it in range(n_it):
             s = it % stages
-            yield ("wait", f"qd_full{s}", it // stages)
+            yield ("wait", f"q_full{s}", it // stages)
+            yield ("wait", f"do_full{s}", it // stages)
             if it > 0 and waits_dq_free:
                 yield ("wait", "dq_free", it - 1)
             qs[h].extend([prod(h, "sdp", it), ("commit", "sp_full")])
             yield ("wait", "p_full", it)
-            qs[h].extend([prod(h, "acc", it), prod(h, "dq", it), ("commit", "dq_full"), ("commit", f"qd_empty{s}")])
+            qs[h].extend([prod(h, "acc", it), prod(h, "dq", it), ("commit", "dq_full"), ("commit", f"q_empty{s}")])
         qs[h].append(("commit", "drain"))
         if h == 0:
             yield ("wait", "drain", 0)
@@ -900,6 +914,13 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
             yield ("wait", "sp_full", it)
             assert cols[0]["sdp"] == it and cols[1]["sdp"] == it, f"pass({it}) finds S/dP {cols[0]['sdp']}, {cols[1]['sdp']}"
             cols[0]["packed"] = cols[1]["packed"] = it
+            # before its first dS store (its own rows) the warp waits for its last block's reductions to have
+            # read both of its tiles; then the dO half of that block's stage can go back to the producer
+            if it > 0:
+                sp = (it - 1) % stages
+                do_tiles[sp].discard(w)
+                if release_after_read:
+                    yield ("arrive", f"do_empty{sp}", 1)
             ds_smem[0] = ("dS", it)
             yield ("arrive", "p_full", 32)
             yield ("wait", "dq_full", it)
@@ -908,6 +929,11 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
             dq_read[1].add((it, w))
             yield ("arrive", "dq_free", 32)
             ds_smem[0] = ("stage", it)
+            s = it % stages
+            assert stage_do[s] == it, f"readout({it}) stages into a dO half holding block {stage_do[s]}"
+            do_tiles[s].add(w)  # pending until this warp's wait at its next pass
+            if not release_after_read:
+                yield ("arrive", f"do_empty{s}", 1)
 
     agents = {"producer": producer(), "w1": issuer(0), "w2": issuer(1)}
     for w in range(8):
@@ -933,7 +959,12 @@ def simulate_bwd128_split(n_it, stages, seed, sp_count=2, dq_count=2, qd_empty_c
         if c == "#tma":
             name, load = tma.pop(rnd.randrange(len(tma)))
             if load is not None:
-                stage[load[0]] = load[1]
+                kind, st, blk = load
+                if kind == "q":
+                    stage_q[st] = blk
+                else:
+                    assert not do_tiles[st], f"dO({blk}) lands on dQ tiles of warps {do_tiles[st]} not yet read"
+                    stage_do[st] = blk
             B[name].arrive(1)
             continue
         try:

@@ -192,7 +192,8 @@ def test_backward_two_issuer_mutations_are_caught(mutation):
 @pytest.mark.parametrize("n_it", [1, 2, 3, 6])
 def test_backward_d128_two_issuer_protocol(n_it):
     """The d = 128 backward with S^T, dV, dQ's first half on one issuing warp and dP^T, dK, dQ's second
-    half on another: the aliased tensor-memory columns always hold the block their reader expects."""
+    half on another: the aliased tensor-memory columns always hold the block their reader expects, and a
+    stage's dO half, which holds dQ tiles until the gradient warps release it, is never refilled early."""
     from pipeline_model import simulate_bwd128_split
 
     for stages in (2, 3):
@@ -200,8 +201,9 @@ def test_backward_d128_two_issuer_protocol(n_it):
             assert simulate_bwd128_split(n_it, stages, seed)
 
 
-@pytest.mark.parametrize("mutation", [{"sp_count": 1}, {"dq_count": 1}, {"qd_empty_count": 1},
-                                      {"waits_dq_free": False}])
+@pytest.mark.parametrize("mutation", [{"sp_count": 1}, {"dq_count": 1}, {"q_empty_count": 1},
+                                      {"waits_dq_free": False}, {"do_empty_count": 7},
+                                      {"release_after_read": False}])
 def test_backward_d128_two_issuer_mutations_are_caught(mutation):
     from pipeline_model import Deadlock, simulate_bwd128_split
 
