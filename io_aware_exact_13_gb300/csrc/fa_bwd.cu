@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // One warp issues only about one product every 77 cycles, so the products are split over two
         // warps: warp 1 issues S^T, dV and dQ's head columns 0..63, warp 2 dP^T, dK and dQ's columns
         // 64..127. Each product's columns are its own warp's (S^T, packed P^T, dQ half 0 in [0, 128);
-        // dP^T, dS^T, dQ half 1 in [128, 256)); sp_full, dq_full, qd_empty and drain take a commit from
+        // dP^T, dS^T, dQ half 1 in [128, 256)); sp_full, dq_full, q_empty and drain take a commit from
         // each warp, and each warp waits dq_free (every product of the last block done and dQ read
         // out) before its next S^T or dP^T overwrites its columns.
         const int h = warp - 1;  // 0: S^T, dV, dQ half 0; 1: dP^T, dK, dQ half 1
