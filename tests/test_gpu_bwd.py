@@ -70,6 +70,8 @@ SMALL = [
     (2, 2, 256, 64, "bf16", True),     # exact multiple of the block
     (1, 1, 1, 128, "bf16", False),     # a single row and key
     (1, 1, 129, 64, "fp16", False),    # one row past a block
+    (1, 2, 700, 128, "fp16", True),    # d = 128 in fp16: causal, ragged tail
+    (2, 1, 640, 128, "fp16", False),   # d = 128 in fp16: five query blocks, the two-stage ring wraps
 ]
 
 
