@@ -177,3 +177,34 @@ def test_bwd_host_validation(fa):
     with pytest.raises(fa.FAError) as e:
         fa.fa_bwd(q96, q96, q96, q96, q96, lse, q96.clone(), q96.clone(), q96.clone(), 0.1, False, ws)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "bf16"), (128, "fp16")])
+def test_bwd_writes_stay_inside_their_buffers(fa, d, dtype):
+    """Guard bands around dQ, dK, dV and the workspace stay untouched (N = 333 is ragged against the
+    128-row blocks, causal), and the gradients still match the oracle."""
+    B, H, N = 2, 2, 333
+    q, k, v, do = make_bwd(B, H, N, d, dtype, seed=333 + d)
+    scale = 1 / math.sqrt(d)
+    dev = torch.device("cuda")
+    ref_o, ref_l = oracle.attention(q, k, v, scale=scale, causal=True)
+    t = DTYPES[dtype]
+    o, lse = torch.from_numpy(ref_o).to(t), torch.from_numpy(ref_l).float()
+    pad = 4096
+    n = B * H * N * d
+    bufs = [torch.full((n + 2 * pad,), 7.0, dtype=t, device=dev) for _ in range(3)]
+    dq, dk, dv = (b[pad:pad + n].view(B, H, N, d) for b in bufs)
+    nws = fa.fa_bwd_workspace_bytes(B, H, N, d)
+    wbuf = torch.full((nws + 2 * pad,), 0x5A, dtype=torch.uint8, device=dev)
+    ws = wbuf[pad:pad + nws]
+    fn = fa.fa_bwd if t == torch.bfloat16 else fa.fa_bwd_fp16
+    fn(q.to(dev), k.to(dev), v.to(dev), o.to(dev), do.to(dev), lse.to(dev), dq, dk, dv, scale, True, ws)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    for b in bufs:
+        assert bool((b[:pad] == 7.0).all()) and bool((b[-pad:] == 7.0).all())
+    assert bool((wbuf[:pad] == 0x5A).all()) and bool((wbuf[-pad:] == 0x5A).all())
+    rq, rk, rv = oracle.attention_bwd(q, k, v, do, scale=scale, causal=True)
+    _cmp("dq", dq, rq)
+    _cmp("dk", dk, rk)
+    _cmp("dv", dv, rv)

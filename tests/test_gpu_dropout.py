@@ -100,3 +100,22 @@ def test_keep_pattern_exactly(fa, d, dtype):
     keep = oracle.dropout_keep(B, H, N, N, p, seed, offset)
     got = out.float().cpu().numpy() != 0.0
     assert np.array_equal(got, keep), f"{int((got != keep).sum())} keep decisions differ"
+
+
+def test_dropout_writes_stay_inside_their_buffers(fa):
+    """Guard bands around O and lse stay untouched (ragged N against the 128-key blocks)."""
+    B, H, N, d = 1, 3, 333, 128
+    q, k, v, _ = make_qkv(B, H, N, d, "bf16", seed=21)
+    pad = 4096
+    obuf = torch.full((B * H * N * d + 2 * pad,), 7.0, dtype=torch.bfloat16, device=DEV)
+    lbuf = torch.full((B * H * N + 2 * pad,), 7.0, dtype=torch.float32, device=DEV)
+    out = obuf[pad:pad + B * H * N * d].view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    fa.fa_fwd_dropout(q.to(DEV), k.to(DEV), v.to(DEV), out, lse, 0.1, True, 0.2, 77, 5)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((obuf[:pad] == 7.0).all()) and bool((obuf[-pad:] == 7.0).all())
+    assert bool((lbuf[:pad] == 7.0).all()) and bool((lbuf[-pad:] == 7.0).all())
+    ref_o, ref_l = oracle.attention_dropout(q, k, v, 0.2, 77, 5, scale=0.1, causal=True)
+    qk = oracle.dropout_threshold(0.2) / 256
+    compare(out, lse, ref_o, ref_l, o_max=2e-2 / qk, o_mean=2e-3 / qk)

@@ -192,3 +192,29 @@ def test_attention_wrapper_uses_the_packed_path(fa):
     with pytest.raises(fa.FAError):
         fa.fa_fwd_masked(q.to(DEV), k.to(DEV), v.to(DEV), mask.to(DEV), o1, l1, 0.1, False,
                          torch.empty(16, dtype=torch.uint8, device=DEV))
+
+
+@pytest.mark.parametrize("d,dtype,causal", [(64, "fp16", True), (128, "bf16", False)])
+def test_masked_writes_stay_inside_their_buffers(fa, d, dtype, causal):
+    """Guard bands around O, lse and the workspace stay untouched: N = 333 is ragged against the
+    128-key blocks and N % 4 != 0 takes the packing pass's scalar loads."""
+    B, H, N = 2, 3, 333
+    q, k, v, mask = make_qkv(B, H, N, d, dtype, seed=N + d, mask_frac=0.2, full_row_frac=0.02)
+    pad = 4096
+    t = q.dtype
+    obuf = torch.full((B * H * N * d + 2 * pad,), 7.0, dtype=t, device=DEV)
+    lbuf = torch.full((B * H * N + 2 * pad,), 7.0, dtype=torch.float32, device=DEV)
+    nws = fa.fa_fwd_masked_workspace_bytes(B, N)
+    wbuf = torch.full((nws + 2 * pad,), 0x5A, dtype=torch.uint8, device=DEV)
+    out = obuf[pad:pad + B * H * N * d].view(B, H, N, d)
+    lse = lbuf[pad:pad + B * H * N].view(B, H, N)
+    ws = wbuf[pad:pad + nws]
+    fn = fa.fa_fwd_masked if q.dtype == torch.bfloat16 else fa.fa_fwd_masked_fp16
+    fn(q.to(DEV), k.to(DEV), v.to(DEV), mask.to(DEV), out, lse, 1 / math.sqrt(d), causal, ws)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    assert bool((obuf[:pad] == 7.0).all()) and bool((obuf[-pad:] == 7.0).all())
+    assert bool((lbuf[:pad] == 7.0).all()) and bool((lbuf[-pad:] == 7.0).all())
+    assert bool((wbuf[:pad] == 0x5A).all()) and bool((wbuf[-pad:] == 0x5A).all())
+    ref_o, ref_l = oracle.attention(q, k, v, mask=mask, scale=1 / math.sqrt(d), causal=causal)
+    compare(out, lse, ref_o, ref_l)
