@@ -242,6 +242,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+    if constexpr (!MASK) {
+        // Launched as a programmatic dependent of the work ahead on the stream: the set-up above overlaps
+        // its tail, and nothing in global memory is read or written before it is complete. The next
+        // forward may likewise be scheduled onto the SMs this grid frees.
+        grid_launch_dependents();
+        grid_dependency_wait();
+    }
 
     if (warp >= 8) {
         setmaxnreg_dec<72>();

@@ -183,13 +183,11 @@ int launch_bk128(const LaunchArgs &a) {
     p.drop_threshold = DROP ? a.drop_threshold : 256;
     p.drop_scale = DROP ? static_cast<float>(256.0 / a.drop_threshold) : 1.0f;
     const int grid = p.n_items < a.num_sms ? p.n_items : a.num_sms;
-    if (MASK)  // behind the packing pass, whose verdict and bits it waits for (the launch gap is saved)
-        return launch_dependent(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, a.stream, tq, tk, tv, p) ==
-                       cudaSuccess
-                   ? 0
-                   : -5;
-    kern<<<grid, kThreads, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    // a programmatic dependent of the work ahead (MASK: the packing pass, whose verdict and bits it waits
+    // for; otherwise whatever ran before, waited for before any global access)
+    return launch_dependent(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, a.stream, tq, tk, tv, p) == cudaSuccess
+               ? 0
+               : -5;
 }
 
 template <typename T, int D, bool VARLEN>
