@@ -170,3 +170,28 @@ def test_side_stream_and_no_allocation(fa):
     assert free0 == free1, "the library must not allocate device memory"
     ref_o, ref_l = oracle.attention(q, k, v, scale=0.1)
     compare(out, lse, ref_o, ref_l)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_back_to_back_calls_that_read_each_others_outputs(fa, d):
+    """The 128-key forward is launched as a programmatic dependent of the work ahead of it and may start
+    before that work ends; it must read nothing in global memory until it has. Three forwards are queued
+    with no synchronisation, each reading the one before's output (O as the next Q, then as K and V),
+    into buffers first filled with a sentinel far from any attention output: a read that came early would
+    see it. Each result is compared with the oracle on the GPU's own inputs."""
+    B, H, N = 1, 4, 700
+    q, k, v, _ = make_qkv(B, H, N, d, "bf16", seed=70 + d)
+    dev = torch.device("cuda")
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    outs = [torch.full((B, H, N, d), 300.0, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    lses = [torch.full((B, H, N), 300.0, dtype=torch.float32, device=dev) for _ in range(3)]
+    fa.fa_fwd(qd, kd, vd, None, outs[0], lses[0], scale, True)
+    fa.fa_fwd(outs[0], kd, vd, None, outs[1], lses[1], scale, True)
+    fa.fa_fwd(outs[1], outs[0], outs[0], None, outs[2], lses[2], scale, False)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status() == fa.FA_OK
+    o0, o1 = outs[0].cpu(), outs[1].cpu()
+    for (qi, ki, vi, causal), o, l in zip([(q, k, v, True), (o0, k, v, True), (o1, o0, o0, False)], outs, lses):
+        ref_o, ref_l = oracle.attention(qi, ki, vi, scale=scale, causal=causal)
+        compare(o, l, ref_o, ref_l)
