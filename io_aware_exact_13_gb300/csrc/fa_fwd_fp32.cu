@@ -12,7 +12,8 @@
 // Layout of the work: 128 threads = 32 rows x 4 threads. The 4 threads of a row
 // split the head dimension in interleaved float4 chunks (chunk 4c + quad), so a
 // warp reads a K or V row from shared memory without bank conflicts; the partial
-// dot products are summed with two shuffles.
+// dot products are summed with two shuffles. The next 32-key K/V tile is loaded
+// into registers while the current one is used.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,6 +36,10 @@ __global__ void __launch_bounds__(kThreadsF32) fa_fwd_fp32_kernel(const float *_
     constexpr int C4 = D / 16;  // float4 chunks per thread
     __shared__ float4 sk[kKeys][D / 4];
     __shared__ float4 sv[kKeys][D / 4];
+    // launched as a programmatic dependent of the work ahead: nothing in global memory is touched before it is
+    // complete; the next forward may be scheduled as this grid's blocks finish
+    grid_launch_dependents();
+    grid_dependency_wait();
     const int bh = blockIdx.y;
     const int b = bh / H;
     const int r0 = blockIdx.x * kRows;
@@ -53,17 +58,32 @@ __global__ void __launch_bounds__(kThreadsF32) fa_fwd_fp32_kernel(const float *_
     }
     float m_run = -INFINITY, l = 0.0f;
     const int key_end = CAUSAL ? min(N, r0 + kRows) : N;
-    for (int j0 = 0; j0 < key_end; j0 += kKeys) {
-        __syncthreads();
-        for (int i = tid; i < kKeys * D / 4; i += kThreadsF32) {
+    // the next K/V tile is loaded into registers while this one is used (PF float4 of each per thread)
+    constexpr int PF = kKeys * D / 4 / kThreadsF32;
+    float4 pk[PF], pv[PF];
+    auto fetch = [&](int j0) {
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            const int i = tid + u * kThreadsF32;
             const int kr = i / (D / 4), kc = i % (D / 4);
             const bool in = j0 + kr < N;
-            sk[kr][kc] = in ? reinterpret_cast<const float4 *>(k + head + (size_t)(j0 + kr) * D)[kc]
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            sv[kr][kc] = in ? reinterpret_cast<const float4 *>(v + head + (size_t)(j0 + kr) * D)[kc]
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            pk[u] = in ? reinterpret_cast<const float4 *>(k + head + (size_t)(j0 + kr) * D)[kc]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            pv[u] = in ? reinterpret_cast<const float4 *>(v + head + (size_t)(j0 + kr) * D)[kc]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    fetch(0);
+    for (int j0 = 0; j0 < key_end; j0 += kKeys) {
+        __syncthreads();  // the last tile's readers are done
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            const int i = tid + u * kThreadsF32;
+            sk[i / (D / 4)][i % (D / 4)] = pk[u];
+            sv[i / (D / 4)][i % (D / 4)] = pv[u];
         }
         __syncthreads();
+        if (j0 + kKeys < key_end) fetch(j0 + kKeys);
         float x[kKeys];
 #pragma unroll
         for (int j = 0; j < kKeys; ++j) {
@@ -126,10 +146,12 @@ template <int D, bool CAUSAL, bool MASK>
 int launch_fp32(const LaunchArgs &a) {
     dim3 grid((a.N + kRows - 1) / kRows, a.B * a.H);
     const float sl2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-    fa_fwd_fp32_kernel<D, CAUSAL, MASK><<<grid, kThreadsF32, 0, a.stream>>>(
-        static_cast<const float *>(a.q), static_cast<const float *>(a.k), static_cast<const float *>(a.v), a.mask,
-        static_cast<float *>(a.out), a.lse, a.H, a.N, sl2);
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    return launch_dependent(fa_fwd_fp32_kernel<D, CAUSAL, MASK>, grid, dim3(kThreadsF32), 0, a.stream,
+                            static_cast<const float *>(a.q), static_cast<const float *>(a.k),
+                            static_cast<const float *>(a.v), a.mask, static_cast<float *>(a.out), a.lse, a.H, a.N,
+                            sl2) == cudaSuccess
+               ? 0
+               : -5;
 }
 
 template <int D>
